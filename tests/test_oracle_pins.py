@@ -1,0 +1,440 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these tests compares the oracle with itself: each checks it against a
+closed form, an invariant, a library routine, a brute-force transcription,
+finite differences, or the pages' own worked example.  ``test_mutants_*``
+plants plausible mistakes in copies of the oracle (on the CPU) and checks
+that at least one pin rejects each of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from oracle import brute, online, ref
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand(shape, seed, sigma=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * sigma
+
+
+# --------------------------------------------------------------------------
+# Pin functions.  Each takes the forward (and backward) under test and returns
+# True when the pin holds.  The real oracle must pass all of them; each planted
+# mutant must fail at least one.
+# --------------------------------------------------------------------------
+
+def pin_three_element(fwd):
+    # [Lecture] "推导 FlashAttention 的在线 softmax": a three-element example of the
+    # incremental numerator/denominator.  The page prints no numbers; scores
+    # (1, 3, 2) with values (1, 2, 3) make the running max change once, then not.
+    q = np.array([[[[1.0]]]])
+    k = np.array([[[[1.0], [3.0], [2.0]]]])
+    v = np.array([[[[1.0], [2.0], [3.0]]]])
+    # Closed form: (e^1*1 + e^3*2 + e^2*3) / (e^1 + e^3 + e^2)
+    closed = (math.e * 1 + math.e ** 3 * 2 + math.e ** 2 * 3) / (math.e + math.e ** 3 + math.e ** 2)
+    lse_closed = math.log(math.e + math.e ** 3 + math.e ** 2)
+    # Query attends to the three keys non-causally; with N=3 every row equals row 0
+    # because q is broadcast -- build q with 3 identical rows.
+    q3 = np.repeat(q, 3, axis=2)
+    o, lse = fwd(q3, k, v, False, 1.0)
+    return abs(o[0, 0, 0, 0] - closed) < 1e-12 and abs(lse[0, 0, 0] - lse_closed) < 1e-12
+
+
+def pin_constant_v(fwd, bwd=None):
+    # A convex combination of identical rows is that row: O_i = c for every i,
+    # causal or not; dQ = dK = 0 because dP is constant along each row.
+    ok = True
+    for causal in (False, True):
+        q = rand((1, 2, 9, 4), 1)
+        k = rand((1, 1, 9, 4), 2)
+        c = rand((4,), 3)
+        v = np.broadcast_to(c, (1, 1, 9, 4)).copy()
+        o, _ = fwd(q, k, v, causal, 0.7)
+        ok &= bool(np.allclose(o, c, atol=1e-12, rtol=0))
+        if bwd is not None:
+            do = rand((1, 2, 9, 4), 4)
+            dq, dk, _ = bwd(q, k, v, do, causal, 0.7)
+            ok &= bool(np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12)
+    return ok
+
+
+def pin_causal_row0(fwd):
+    # [Lecture] "GPU 显存和注意力瓶颈": in causal self-attention a token attends to
+    # itself and earlier tokens, so token 0 sees only key 0: O_0 = v_0, LSE_0 = s*q0.k0.
+    q = rand((1, 1, 6, 5), 5)
+    k = rand((1, 1, 6, 5), 6)
+    v = rand((1, 1, 6, 5), 7)
+    o, lse = fwd(q, k, v, True, 0.5)
+    return (np.allclose(o[0, 0, 0], v[0, 0, 0], atol=1e-12, rtol=0)
+            and abs(lse[0, 0, 0] - 0.5 * q[0, 0, 0] @ k[0, 0, 0]) < 1e-12)
+
+
+def pin_zero_q(fwd):
+    # Q = 0 makes every visible score 0: uniform weights.  Non-causal: mean of V,
+    # LSE = ln N.  Causal: prefix means, LSE_i = ln(i + 1).
+    N = 7
+    q = np.zeros((1, 1, N, 3))
+    k = rand((1, 1, N, 3), 8)
+    v = rand((1, 1, N, 3), 9)
+    o, lse = fwd(q, k, v, False, 1.0)
+    ok = np.allclose(o[0, 0], v[0, 0].mean(axis=0), atol=1e-12) and np.allclose(lse, math.log(N))
+    o, lse = fwd(q, k, v, True, 1.0)
+    prefix = np.cumsum(v[0, 0], axis=0) / np.arange(1, N + 1)[:, None]
+    ok &= np.allclose(o[0, 0], prefix, atol=1e-12) and np.allclose(lse[0, 0], np.log(np.arange(1, N + 1)))
+    return bool(ok)
+
+
+def pin_lse_library(fwd):
+    # LSE_i = ln sum_j exp(s * q_i . k_j) over visible j, against scipy's logsumexp.
+    q = rand((2, 2, 11, 6), 10, 3.0)
+    k = rand((2, 2, 11, 6), 11, 3.0)
+    v = rand((2, 2, 11, 6), 12)
+    ok = True
+    for causal in (False, True):
+        _, lse = fwd(q, k, v, causal, 0.3)
+        for b in range(2):
+            for h in range(2):
+                s = 0.3 * q[b, h] @ k[b, h].T
+                if causal:
+                    s = np.where(np.tril(np.ones((11, 11), bool)), s, -np.inf)
+                ok &= bool(np.allclose(lse[b, h], scipy.special.logsumexp(s, axis=1), atol=1e-12, rtol=1e-13))
+    return ok
+
+
+def pin_torch_sdpa(fwd, bwd):
+    # The definition reduces to torch's scaled_dot_product_attention run on the CPU
+    # in fp64 (a library routine, with autograd for the backward); GQA via repeat.
+    B, Hq, Hkv, N, d = 2, 4, 2, 10, 8
+    q = rand((B, Hq, N, d), 13)
+    k = rand((B, Hkv, N, d), 14)
+    v = rand((B, Hkv, N, d), 15)
+    do = rand((B, Hq, N, d), 16)
+    ok = True
+    for causal in (False, True):
+        tq = torch.tensor(q, requires_grad=True)
+        tk = torch.tensor(k, requires_grad=True)
+        tv = torch.tensor(v, requires_grad=True)
+        rk = tk.repeat_interleave(Hq // Hkv, dim=1)
+        rv = tv.repeat_interleave(Hq // Hkv, dim=1)
+        to = torch.nn.functional.scaled_dot_product_attention(tq, rk, rv, is_causal=causal, scale=0.35)
+        to.backward(torch.tensor(do))
+        o, _ = fwd(q, k, v, causal, 0.35)
+        dq, dk, dv = bwd(q, k, v, do, causal, 0.35)
+        ok &= bool(np.allclose(o, to.detach().numpy(), atol=1e-12, rtol=1e-10))
+        ok &= bool(np.allclose(dq, tq.grad.numpy(), atol=1e-11, rtol=1e-9))
+        ok &= bool(np.allclose(dk, tk.grad.numpy(), atol=1e-11, rtol=1e-9))
+        ok &= bool(np.allclose(dv, tv.grad.numpy(), atol=1e-11, rtol=1e-9))
+    return ok
+
+
+def pin_gqa(fwd, bwd):
+    # [Lecture] "减少缓存表示并验证草稿": G key/value groups shared by H query heads.
+    # Grouped attention equals multi-head attention on K/V heads repeated per group,
+    # and the grouped dK/dV are the sums of the repeated heads' gradients.
+    B, Hq, Hkv, N, d = 1, 6, 2, 7, 4
+    q = rand((B, Hq, N, d), 17)
+    k = rand((B, Hkv, N, d), 18)
+    v = rand((B, Hkv, N, d), 19)
+    do = rand((B, Hq, N, d), 20)
+    rk = np.repeat(k, Hq // Hkv, axis=1)
+    rv = np.repeat(v, Hq // Hkv, axis=1)
+    ok = True
+    for causal in (False, True):
+        o, lse = fwd(q, k, v, causal, 0.5)
+        o2, lse2 = fwd(q, rk, rv, causal, 0.5)
+        ok &= bool(np.allclose(o, o2, atol=1e-13) and np.allclose(lse, lse2, atol=1e-13))
+        dq, dk, dv = bwd(q, k, v, do, causal, 0.5)
+        dq2, dk2, dv2 = bwd(q, rk, rv, do, causal, 0.5)
+        dk2 = dk2.reshape(B, Hkv, Hq // Hkv, N, d).sum(axis=2)
+        dv2 = dv2.reshape(B, Hkv, Hq // Hkv, N, d).sum(axis=2)
+        ok &= bool(np.allclose(dq, dq2, atol=1e-13) and np.allclose(dk, dk2, atol=1e-13)
+                   and np.allclose(dv, dv2, atol=1e-13))
+    return ok
+
+
+def _fd_case(fwd, bwd, B, Hq, Hkv, N, d, causal, seed, h=1e-6):
+    scale = 0.6
+    q = rand((B, Hq, N, d), seed)
+    k = rand((B, Hkv, N, d), seed + 1)
+    v = rand((B, Hkv, N, d), seed + 2)
+    do = rand((B, Hq, N, d), seed + 3)
+    dq, dk, dv = bwd(q, k, v, do, causal, scale)
+
+    def loss(qq, kk, vv):
+        return float(np.sum(do * fwd(qq, kk, vv, causal, scale)[0]))
+
+    worst = 0.0
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            xp = x.copy(); xp[idx] += h
+            xm = x.copy(); xm[idx] -= h
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        denom = max(1e-3, float(np.abs(num).max()))
+        worst = max(worst, float(np.abs(num - g).max()) / denom)
+    return worst
+
+
+FD_CASES = [
+    (1, 1, 1, 1, 3, False), (1, 1, 1, 5, 4, True), (1, 2, 1, 8, 3, True),
+    (1, 2, 2, 5, 4, False), (1, 2, 1, 8, 4, False),
+]
+
+
+def pin_finite_differences(fwd, bwd):
+    # The pages give no backward formulas; the backward is the calculus of the
+    # forward definition.  Central differences of L = sum(dO * O) pin it.
+    return all(_fd_case(fwd, bwd, *c, seed=30 + i) <= 1e-6 for i, c in enumerate(FD_CASES))
+
+
+def to_list(a):
+    return a.tolist()
+
+
+def pin_brute(fwd, bwd):
+    ok = True
+    for (B, Hq, Hkv, N, d, causal, seed) in [(1, 1, 1, 1, 2, False, 40), (1, 2, 1, 6, 3, True, 41),
+                                             (2, 2, 2, 5, 4, False, 42), (1, 4, 2, 7, 2, True, 43)]:
+        q = rand((B, Hq, N, d), seed)
+        k = rand((B, Hkv, N, d), seed + 1)
+        v = rand((B, Hkv, N, d), seed + 2)
+        do = rand((B, Hq, N, d), seed + 3)
+        o, lse = fwd(q, k, v, causal, 0.45)
+        bo, blse = brute.forward(to_list(q), to_list(k), to_list(v), causal, 0.45)
+        ok &= bool(np.allclose(o, bo, atol=1e-12) and np.allclose(lse, blse, atol=1e-12))
+        dq, dk, dv = bwd(q, k, v, do, causal, 0.45)
+        bdq, bdk, bdv = brute.backward(to_list(q), to_list(k), to_list(v), to_list(do), causal, 0.45)
+        ok &= bool(np.allclose(dq, bdq, atol=1e-12) and np.allclose(dk, bdk, atol=1e-12)
+                   and np.allclose(dv, bdv, atol=1e-12))
+    return ok
+
+
+ALL_PINS = [pin_three_element, pin_constant_v, pin_causal_row0, pin_zero_q, pin_lse_library,
+            pin_torch_sdpa, pin_gqa, pin_finite_differences, pin_brute]
+
+
+def run_pin(pin, fwd, bwd):
+    import inspect
+    n = len(inspect.signature(pin).parameters)
+    try:
+        return pin(fwd, bwd) if n == 2 else pin(fwd)
+    except (FloatingPointError, ValueError, IndexError):
+        return False
+
+
+# --------------------------------------------------------------------------
+# The oracle passes every pin.
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(pin):
+    with np.errstate(all="ignore"):
+        assert run_pin(pin, ref.attention_forward, ref.attention_backward)
+
+
+def test_row_block_partition_is_exact():
+    # Row blocking only partitions independent rows: any block size gives the same result.
+    q, k, v, do = (rand((1, 2, 37, 5), s) for s in (50, 51, 52, 53))
+    for causal in (False, True):
+        o1, l1 = ref.attention_forward(q, k, v, causal, 0.4, row_block=37)
+        o2, l2 = ref.attention_forward(q, k, v, causal, 0.4, row_block=4)
+        # (BLAS may sum in a different order for different block heights.)
+        assert np.allclose(o1, o2, atol=1e-14) and np.allclose(l1, l2, atol=1e-14)
+        g1 = ref.attention_backward(q, k, v, do, causal, 0.4, row_block=37)
+        g2 = ref.attention_backward(q, k, v, do, causal, 0.4, row_block=3)
+        for a, b in zip(g1, g2):
+            assert np.allclose(a, b, atol=1e-14)
+
+
+def test_probability_rows_sum_to_one():
+    s = rand((64, 300), 60, 9.0)
+    s[:, 200:] = -np.inf
+    p, _, _ = ref.softmax_rows(s)
+    assert np.all(p >= 0)
+    assert np.max(np.abs(p.sum(axis=1) - 1.0)) <= 1e-12
+    assert np.all(p[:, 200:] == 0)
+
+
+# --------------------------------------------------------------------------
+# The pages' streaming recurrence, pinned by the worked example and against the
+# two-pass definition.
+# --------------------------------------------------------------------------
+
+def test_three_element_stream_states():
+    trace = []
+    num, den, m = online.stream([1.0, 3.0, 2.0], [1.0, 2.0, 3.0], block=1, trace=trace)
+    # After element 1: the running max is that score; num = den = exp(0) = 1.
+    assert trace[0] == (1.0, 1.0, 1.0)
+    # After element 2: max rises to 3; old sums are rescaled by exp(1 - 3).
+    f = math.exp(-2.0)
+    assert trace[1][0] == 3.0
+    assert abs(trace[1][1] - (1.0 * f + 2.0)) < 1e-15
+    assert abs(trace[1][2] - (1.0 * f + 1.0)) < 1e-15
+    # After element 3: the max stays 3 (factor 1); exp(2 - 3) is added.
+    g = math.exp(-1.0)
+    assert abs(num - (f + 2.0 + 3.0 * g)) < 1e-15
+    assert abs(den - (f + 1.0 + g)) < 1e-15
+    closed = (math.e + 2 * math.e ** 3 + 3 * math.e ** 2) / (math.e + math.e ** 3 + math.e ** 2)
+    assert abs(num / den - closed) < 1e-14
+    assert abs(num / den - 2.154697897884) < 1e-11
+    assert abs(m + math.log(den) - 3.407605964444) < 1e-11
+
+
+@pytest.mark.parametrize("sigma", [1.0, 9.0])
+def test_online_equals_two_pass(sigma):
+    rng = np.random.default_rng(int(sigma * 10))
+    for n in (1, 2, 3, 17, 128, 129, 1000, 4096):
+        s = rng.standard_normal(n) * sigma
+        vals = rng.standard_normal((n, 3))
+        p, m, den = ref.softmax_rows(s[None, :])
+        two_pass = p[0] @ vals
+        for block in (1, 7, 128, n):
+            got = online.softmax_weighted_sum(list(s), vals.tolist(), block=block)
+            assert np.allclose(got, two_pass, rtol=1e-12, atol=1e-12)
+            assert abs(online.log_sum_exp(list(s), block) - scipy.special.logsumexp(s)) <= 1e-12 * max(1, abs(m[0]))
+
+
+def test_rescale_identity():
+    # Multiplying numerator and denominator by one factor leaves their ratio
+    # unchanged: a stale reference max (any c >= true max) gives the same output.
+    rng = np.random.default_rng(70)
+    s = rng.standard_normal(50) * 4
+    v = rng.standard_normal(50)
+    exact = scipy.special.softmax(s) @ v
+    for c in (s.max(), s.max() + 3.0, s.max() + 20.0):
+        w = np.exp(s - c)
+        assert abs((w @ v) / w.sum() - exact) < 1e-12
+
+
+def test_d_identity():
+    # rowsum(dO * O) equals rowsum(P * dP): the backward's row term can be formed
+    # from the forward output instead of the probabilities.
+    q, k, v, do = (rand((1, 1, 12, 5), s) for s in (80, 81, 82, 83))
+    for causal in (False, True):
+        o, _ = ref.attention_forward(q, k, v, causal, 0.5)
+        s = 0.5 * q[0, 0] @ k[0, 0].T
+        if causal:
+            s = np.where(np.tril(np.ones((12, 12), bool)), s, -np.inf)
+        p, _, _ = ref.softmax_rows(s)
+        dp = do[0, 0] @ v[0, 0].T
+        assert np.allclose((do[0, 0] * o[0, 0]).sum(1), (p * dp).sum(1), atol=1e-13)
+
+
+def test_stressed_logits_stay_finite():
+    # Large logits (q, k ~ N(0, 3^2), as in the stressed workload) stay finite
+    # because the max is subtracted before exp.
+    q = rand((1, 1, 64, 64), 90, 3.0)
+    k = rand((1, 1, 64, 64), 91, 3.0)
+    v = rand((1, 1, 64, 64), 92)
+    o, lse = ref.attention_forward(q, k, v, False, 1 / 8)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    s = q[0, 0] @ k[0, 0].T / 8
+    assert np.allclose(lse[0, 0], scipy.special.logsumexp(s, axis=1), rtol=1e-13)
+
+
+def test_page_printed_sizes():
+    # The avoided N x N buffers have the sizes the pages print.
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "score_matrix_sizes.txt"))
+            if l.strip() and not l.startswith("#")]
+    table = {r[0]: r[1:] for r in rows}
+    h, n, bpe, val, unit = table["qkt_8k_fp32"]
+    nbytes = int(h) * int(n) ** 2 * int(bpe)
+    assert abs(nbytes / 2 ** 20 - float(val)) / float(val) < 0.05  # 256 MiB
+    h, n, bpe, val, unit = table["sp_h32_l4096_fp32"]
+    nbytes = int(h) * int(n) ** 2 * int(bpe)
+    assert abs(nbytes / 1e9 - float(val)) / float(val) < 0.05  # 2.1 GB
+    hq, hkv, _, val, unit = table["gqa_24q_2kv_saving"]
+    # K/V storage scales with the number of kv heads that ref.kv_head_index reads.
+    used = {ref.kv_head_index(h, int(hq), int(hkv)) for h in range(int(hq))}
+    saving = 100 * (1 - len(used) / int(hq))
+    assert abs(saving - float(val)) < 1.0
+
+
+# --------------------------------------------------------------------------
+# Planted mistakes: each plausible error in a copy of the oracle fails a pin.
+# --------------------------------------------------------------------------
+
+def _mut_bwd_no_rowterm(q, k, v, do, causal, scale):
+    # dS = P * dP (the rowsum(P*dP) term dropped)
+    dq = np.zeros_like(q); dk = np.zeros_like(k); dv = np.zeros_like(v)
+    B, Hq, N, d = q.shape; Hkv = k.shape[1]
+    for b in range(B):
+        for h in range(Hq):
+            g = ref.kv_head_index(h, Hq, Hkv)
+            s = scale * q[b, h] @ k[b, g].T
+            s = np.where(ref.visible_mask(np.arange(N), N, causal), s, -np.inf)
+            p, _, _ = ref.softmax_rows(s)
+            dv[b, g] += p.T @ do[b, h]
+            ds = p * (do[b, h] @ v[b, g].T)
+            dq[b, h] = scale * ds @ k[b, g]
+            dk[b, g] += scale * ds.T @ q[b, h]
+    return dq, dk, dv
+
+
+def _mut_bwd_sign(q, k, v, do, causal, scale):
+    dq, dk, dv = ref.attention_backward(q, k, v, do, causal, scale)
+    return -dq, dk, dv
+
+
+def _mut_bwd_dk_unscaled(q, k, v, do, causal, scale):
+    dq, dk, dv = ref.attention_backward(q, k, v, do, causal, scale)
+    return dq, dk / scale, dv
+
+
+MUTANTS = {
+    "dropped_scale": (lambda q, k, v, c, s, **kw: ref.attention_forward(q, k, v, c, 1.0),
+                      ref.attention_backward),
+    "v_replaced_by_k": (lambda q, k, v, c, s, **kw: ref.attention_forward(q, k, k, c, s),
+                        ref.attention_backward),
+    "lse_without_max": (lambda q, k, v, c, s, **kw: (ref.attention_forward(q, k, v, c, s)[0],
+                                                     ref.attention_forward(q, k, v, c, s)[1]
+                                                     - ref.attention_forward(q, k, v, c, s)[1].max()),
+                        ref.attention_backward),
+    "bwd_dropped_row_term": (ref.attention_forward, _mut_bwd_no_rowterm),
+    "bwd_sign": (ref.attention_forward, _mut_bwd_sign),
+    "bwd_dk_unscaled": (ref.attention_forward, _mut_bwd_dk_unscaled),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutants_are_caught(name):
+    fwd, bwd = MUTANTS[name]
+    with np.errstate(all="ignore"):
+        results = {p.__name__: run_pin(p, fwd, bwd) for p in ALL_PINS}
+    assert not all(results.values()), f"mutant {name} passed every pin"
+
+
+def test_mutant_gqa_mapping_is_caught(monkeypatch):
+    # Interleaved instead of contiguous head groups.
+    monkeypatch.setattr(ref, "kv_head_index", lambda h, Hq, Hkv: h % Hkv)
+    with np.errstate(all="ignore"):
+        assert not run_pin(pin_gqa, ref.attention_forward, ref.attention_backward) or \
+            not run_pin(pin_torch_sdpa, ref.attention_forward, ref.attention_backward)
+
+
+def test_mutant_strict_causal_is_caught(monkeypatch):
+    # Query i seeing only keys j < i (itself excluded).
+    monkeypatch.setattr(ref, "visible_mask",
+                        lambda rows, N, causal: (np.arange(N)[None, :] < rows[:, None]) if causal
+                        else np.ones((len(rows), N), bool))
+    with np.errstate(all="ignore"):
+        assert not run_pin(pin_causal_row0, ref.attention_forward, ref.attention_backward)
+
+
+def test_mutant_off_by_one_causal_is_caught(monkeypatch):
+    # Query i also seeing key i + 1.
+    monkeypatch.setattr(ref, "visible_mask",
+                        lambda rows, N, causal: (np.arange(N)[None, :] <= rows[:, None] + 1) if causal
+                        else np.ones((len(rows), N), bool))
+    with np.errstate(all="ignore"):
+        assert not run_pin(pin_causal_row0, ref.attention_forward, ref.attention_backward)
