@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Benchmark of the exact-attention hot path on GB300: one step = forward +
+backward (fa_fwd, then fa_bwd's three kernels) over one batch of synthetic
+bf16 inputs of the standard causal training shape (B=4, Hq=Hkv=16, N=2048,
+d=128).
+
+Prints ONE JSON line (rank 0).  `value` is TFLOPS under the convention
+fwd = 4*B*Hq*N^2*d (halved when causal), bwd = 2.5 x fwd, over the device time
+of the K timed steps (CUDA events around each step on the launching stream;
+L2 is flushed by a 256 MiB write between steps, outside the events).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (fp64 NumPy) on the host cores: each
+step is a bounded sample of the same workload (one block of query rows of one
+head, forward + backward), reported in the same unit.
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+on its own GPU (weak scaling, no collective on the data path); the time is
+the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_io_aware_flashattention_gb300.inputs import BENCH_WORKLOAD, WORKLOADS, make_workload_inputs  # noqa: E402
+
+L2_FLUSH_BYTES = 256 * 2 ** 20
+FALLBACK_BF16_TFLOPS = 1900.0
+DOMINANT_KERNEL = "fa_bwd_dkdv_kernel"
+METRIC = "attention fwd/bwd TFLOPS (bf16, causal) and % of GB300 dense-bf16 peak, 1 GPU"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+# ---------------------------------------------------------------------------
+# measured peaks, kernel source hash, ncu traffic record
+# ---------------------------------------------------------------------------
+
+def bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement)"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_io_aware_flashattention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload, src_hash):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    if there is none for this workload or the kernel sources changed since."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+        e = rec[kernel][workload]
+        if e.get("source_hash") != src_hash:
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(os.devnull, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=self.out, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            text, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            text, _ = self.proc.communicate()
+        rows = [[c.strip() for c in l.split(",")] for l in text.strip().splitlines() if l.count(",") >= 9]
+        if self.bus_id:
+            mine = [r for r in rows if r[1].lower().endswith(self.bus_id[-12:])]
+            rows = mine or rows
+        if rows and not self.bus_id:
+            first = rows[0][0]
+            rows = [r for r in rows if r[0] == first]
+        sm = [float(r[2].split()[0]) for r in rows if r[2].split()[0].replace(".", "").isdigit()]
+        mx = [float(r[3].split()[0]) for r in rows if r[3].split()[0].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle sample (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_plan(w, rows_per_sample=128):
+    """Row blocks (b, h, r0, r1) of the workload, spread over the sequence."""
+    import numpy as np
+    rng = np.random.default_rng(12345)
+    nblk = w.N // rows_per_sample if w.N >= rows_per_sample else 1
+    while True:
+        b = int(rng.integers(w.B))
+        h = int(rng.integers(w.Hq))
+        blk = int(rng.integers(nblk))
+        r0 = blk * rows_per_sample
+        yield b, h, r0, min(w.N, r0 + rows_per_sample)
+
+
+def sample_flops(w, r0, r1):
+    """Convention FLOPs (fwd + bwd) of query rows r0..r1-1 of one head."""
+    if w.causal:
+        pairs = sum(i + 1 for i in range(r0, r1))
+    else:
+        pairs = (r1 - r0) * w.N
+    return 4.0 * w.d * pairs * 3.5
+
+
+def run_oracle_sample(w, tensors, b, h, r0, r1):
+    from oracle import ref
+    q, k, v, do = tensors
+    g = h // (w.Hq // w.Hkv)
+    sub = (q[b:b + 1, h:h + 1], k[b:b + 1, g:g + 1], v[b:b + 1, g:g + 1])
+    ref.attention_forward(*sub, w.causal, w.scale, row_range=(r0, r1))
+    ref.attention_backward(*sub, do[b:b + 1, h:h + 1], w.causal, w.scale, row_range=(r0, r1))
+
+
+def f64_tensors(w):
+    q, k, v, do = make_workload_inputs(w)
+    return tuple(t.to(__import__("torch").float64).numpy() for t in (q, k, v, do))
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, tensors, budget_s=12.0):
+    plan = oracle_sample_plan(w)
+    flops = 0.0
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        b, h, r0, r1 = next(plan)
+        run_oracle_sample(w, tensors, b, h, r0, r1)
+        flops += sample_flops(w, r0, r1)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{n} blocks of 128 query rows (one head each, fwd+bwd, fp64 NumPy), {dt:.1f} s"}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    tensors = f64_tensors(w)
+    plan = oracle_sample_plan(w)
+    for _ in range(args.warmup):
+        run_oracle_sample(w, tensors, *next(plan))
+    flops = 0.0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        b, h, r0, r1 = next(plan)
+        run_oracle_sample(w, tensors, b, h, r0, r1)
+        flops += sample_flops(w, r0, r1)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / max(1, args.steps) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"each step: one block of 128 query rows of one head, forward + backward, "
+                                   f"fp64 NumPy oracle; {args.steps} steps"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
+            "scale": w.scale, "global_batch": w.B, "seq_len": w.N,
+            "l2": "flushed between steps (256 MiB write outside the timed events)",
+            "parallelism": "replicas (one independent workload per GPU)"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w):
+    import torch
+    import exact_io_aware_flashattention_gb300 as fa
+    from exact_io_aware_flashattention_gb300 import _build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device() if world == 1 else local)
+    if rank == 0 or world > 1:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    fa.load_library()
+
+    q_h, k_h, v_h, do_h = make_workload_inputs(w)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    B, Hq, Hkv, N, d = w.B, w.Hq, w.Hkv, w.N, w.d
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa.fa_bwd_workspace_bytes(B, Hq, Hkv, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    ptr = lambda t: t.data_ptr()  # noqa: E731
+
+    def call(status, what):
+        if status != 0:
+            raise fa.FAError(status, what)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        call(fa.fa_fwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, Hq, Hkv, N, d, w.causal, w.scale, sh), "fwd")
+        if ev:
+            ev[1].record(stream)
+        call(fa.fa_bwd_preprocess(ptr(o), ptr(do), B, Hq, Hkv, N, d, ptr(ws), ws_bytes, sh), "bwd_preprocess")
+        if ev:
+            ev[2].record(stream)
+        call(fa.fa_bwd_dkdv(ptr(q), ptr(k), ptr(v), ptr(do), ptr(lse), ptr(dk), ptr(dv), B, Hq, Hkv, N, d,
+                            w.causal, w.scale, ptr(ws), ws_bytes, sh), "bwd_dkdv")
+        if ev:
+            ev[3].record(stream)
+        call(fa.fa_bwd_dq_convert(ptr(dq), B, Hq, Hkv, N, d, w.scale, ptr(ws), ws_bytes, sh), "bwd_dq_convert")
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    fa.check_device_status()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.25)  # let the sampler attach before the timed region
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    fa.check_device_status()
+
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in events]
+    pre_ms = [e[1].elapsed_time(e[2]) for e in events]
+    dkdv_ms = [e[2].elapsed_time(e[3]) for e in events]
+    conv_ms = [e[3].elapsed_time(e[4]) for e in events]
+    step_ms = [e[0].elapsed_time(e[4]) for e in events]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    step_flops = w.fwd_flops + w.bwd_flops
+    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+
+    peak, peak_src = bf16_peak()
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_avg = statistics.mean(p + k_ + c for p, k_, c in zip(pre_ms, dkdv_ms, conv_ms))
+    dkdv_avg = statistics.mean(dkdv_ms)
+    fwd_tflops = w.fwd_flops / (fwd_avg * 1e-3) / 1e12
+    bwd_tflops = w.bwd_flops / (bwd_avg * 1e-3) / 1e12
+    dkdv_tflops = w.bwd_flops / (dkdv_avg * 1e-3) / 1e12
+    if dkdv_avg >= fwd_avg:
+        dom, dom_flops, dom_ms = "fa_bwd_dkdv_kernel", w.bwd_flops, dkdv_avg
+    else:
+        dom, dom_flops, dom_ms = "fa_fwd_kernel", w.fwd_flops, fwd_avg
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    src_hash = kernel_source_hash()
+
+    # ---------------- e2e through host buffers (pinned), copies inside the timed region
+    e2e = None
+    if rank == 0 or world > 1:
+        pin = lambda t: t.pin_memory()  # noqa: E731
+        hq, hk, hv, hdo = pin(q_h), pin(k_h), pin(v_h), pin(do_h)
+        ho, hlse = pin(torch.empty_like(q_h)), pin(torch.empty((B, Hq, N), dtype=torch.float32))
+        hdq, hdk, hdv = pin(torch.empty_like(q_h)), pin(torch.empty_like(k_h)), pin(torch.empty_like(v_h))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            do.copy_(hdo, non_blocking=True)
+            fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+            fa.backward(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, workspace=ws, dq=dq, dk=dk, dv=dv)
+            ho.copy_(o, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            hdq.copy_(dq, non_blocking=True)
+            hdk.copy_(dk, non_blocking=True)
+            hdv.copy_(dv, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, min(args.steps, 50))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        fa.check_device_status()
+        e2e = {"value": step_flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "steps": n_e2e, "path": "pinned host -> fa.forward/fa.backward (C ABI) -> pinned host"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, f64_tensors(w))
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w),
+            "fwd": {"tflops": fwd_tflops, "ms": fwd_avg, "frac_of_peak": fwd_tflops / peak},
+            "bwd": {"tflops": bwd_tflops, "ms": bwd_avg, "frac_of_peak": bwd_tflops / peak,
+                    "ms_preprocess": statistics.mean(pre_ms), "ms_dkdv": dkdv_avg,
+                    "ms_dq_convert": statistics.mean(conv_ms)},
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
+                         "traffic": ncu_traffic(dom, w.name, src_hash),
+                         "algorithmic_flops_per_launch": dom_flops},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": 4 * args.steps,
+            "wall_s_timed_region": wall,
+            "kernel_source_hash": src_hash,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

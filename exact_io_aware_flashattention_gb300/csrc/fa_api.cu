@@ -1,0 +1,341 @@
+// C-ABI layer of libfa_gb300.so: argument validation, TMA tensor maps,
+// kernel launches and the device status words.  See include/fa.h for the
+// contract of every entry point.
+#include "fa.h"
+
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace {
+
+// First device-side error: code, block, wait site, thread.  Read and cleared
+// by fa_last_device_status.
+__device__ int g_status_words[4];
+
+__global__ void wait_selftest_kernel(fa::DevStatus st) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    fa::mbar_init(&bar, 1);
+    abort_flag = 0;
+    fa::mbar_fence_init();
+  }
+  __syncthreads();
+  // Nothing ever arrives on `bar`: the bounded wait must give up and record
+  // FA_ERR_DEVICE_TIMEOUT.
+  if (threadIdx.x == 0) fa::mbar_wait(&bar, 0, st, &abort_flag, 99);
+  __syncthreads();
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+unsigned long long default_timeout_ns() {
+  static unsigned long long t = [] {
+    const char* s = std::getenv("FA_WAIT_TIMEOUT_NS");
+    unsigned long long v = s ? std::strtoull(s, nullptr, 10) : 0ull;
+    return v ? v : 2000000000ull;  // 2 s: far above any single wait of a correct run
+  }();
+  return t;
+}
+
+fa_status device_state(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED_DEVICE;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_words) != cudaSuccess) return FA_ERR_CUDA;
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return FA_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    s.num_sms = sms;
+    s.status = static_cast<int*>(p);
+    s.ready = true;
+  }
+  *out = &s;
+  return FA_OK;
+}
+
+fa::DevStatus dev_status(const DeviceState* s) { return fa::DevStatus{s->status, default_timeout_ns()}; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_shape(int B, int Hq, int Hkv, int N, int d) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return FA_ERR_BAD_SHAPE;
+  if (Hq % Hkv != 0) return FA_ERR_BAD_SHAPE;
+  if (B > 65535 || N > 65535 * 128) return FA_ERR_BAD_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_HEADDIM;
+  return FA_OK;
+}
+
+fa_status check_scale(int causal, float scale) {
+  if (causal != 0 && causal != 1) return FA_ERR_BAD_ARGUMENT;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_ARGUMENT;
+  return FA_OK;
+}
+
+struct Range {
+  uintptr_t lo, hi;
+};
+Range range(const void* p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + bytes};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t elems(int B, int H, int N, int d) { return (size_t)B * H * N * d; }
+
+struct WsLayout {
+  size_t dq_off, dr_off, total;
+};
+WsLayout ws_layout(int B, int Hq, int N, int d) {
+  WsLayout w;
+  w.dq_off = 0;
+  w.dr_off = align256(elems(B, Hq, N, d) * 4);
+  w.total = w.dr_off + align256((size_t)B * Hq * N * 4);
+  return w;
+}
+
+fa_status tmap_bf16(CUtensorMap* m, const void* base, int B, int H, int N, int d) {
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2, (cuuint64_t)H * N * d * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_LAUNCH;
+}
+
+fa_status launch_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH; }
+
+#define FA_TRY(x)                   \
+  do {                              \
+    fa_status _s = (x);             \
+    if (_s != FA_OK) return _s;     \
+  } while (0)
+
+fa_status validate_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse, void* dk,
+                        void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                        const void* workspace, size_t workspace_bytes) {
+  if (!q || !k || !v || !dO || !lse || !dk || !dv || !workspace) return FA_ERR_NULL_PTR;
+  FA_TRY(check_shape(B, Hq, Hkv, N, d));
+  FA_TRY(check_scale(causal, scale));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) || !aligned16(dk) ||
+      !aligned16(dv) || !aligned16(workspace))
+    return FA_ERR_MISALIGNED;
+  if (workspace_bytes < ws_layout(B, Hq, N, d).total) return FA_ERR_WORKSPACE_TOO_SMALL;
+  const size_t qb = elems(B, Hq, N, d) * 2, kb = elems(B, Hkv, N, d) * 2;
+  const Range ins[] = {range(q, qb), range(k, kb), range(v, kb), range(dO, qb), range(lse, (size_t)B * Hq * N * 4)};
+  const Range outs[] = {range(dk, kb), range(dv, kb), range(workspace, ws_layout(B, Hq, N, d).total)};
+  for (const Range& o : outs)
+    for (const Range& i : ins)
+      if (overlap(o, i)) return FA_ERR_ALIASING;
+  if (overlap(outs[0], outs[1]) || overlap(outs[0], outs[2]) || overlap(outs[1], outs[2])) return FA_ERR_ALIASING;
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_strerror(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_NULL_PTR: return "a required pointer is NULL";
+    case FA_ERR_BAD_SHAPE: return "bad shape (B, Hq, Hkv, N must be >= 1, Hq % Hkv == 0, B <= 65535, N <= 8388480)";
+    case FA_ERR_UNSUPPORTED_HEADDIM: return "unsupported head dimension (d must be 64 or 128)";
+    case FA_ERR_MISALIGNED: return "a pointer is not 16-byte aligned";
+    case FA_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than fa_bwd_workspace_bytes()";
+    case FA_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3 (GB300)";
+    case FA_ERR_LAUNCH: return "kernel launch or tensor-map encoding failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "a device-side bounded wait ran out";
+    case FA_ERR_CUDA: return "CUDA runtime error";
+    case FA_ERR_BAD_ARGUMENT: return "bad argument (scale must be finite and > 0, causal 0 or 1)";
+    case FA_ERR_ALIASING: return "an output overlaps an input or another output";
+  }
+  return "unknown status";
+}
+
+size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
+  if (check_shape(B, Hq, Hkv, N, d) != FA_OK) return 0;
+  return ws_layout(B, Hq, N, d).total;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                 int d, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_PTR;
+  FA_TRY(check_shape(B, Hq, Hkv, N, d));
+  FA_TRY(check_scale(causal, scale));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
+  const size_t qb = elems(B, Hq, N, d) * 2, kb = elems(B, Hkv, N, d) * 2;
+  const Range ins[] = {range(q, qb), range(k, kb), range(v, kb)};
+  const Range ro = range(o, qb), rl = range(lse, (size_t)B * Hq * N * 4);
+  for (const Range& i : ins)
+    if (overlap(ro, i) || overlap(rl, i)) return FA_ERR_ALIASING;
+  if (overlap(ro, rl)) return FA_ERR_ALIASING;
+
+  DeviceState* ds = nullptr;
+  FA_TRY(device_state(&ds));
+  CUtensorMap tq, tk, tv;
+  FA_TRY(tmap_bf16(&tq, q, B, Hq, N, d));
+  FA_TRY(tmap_bf16(&tk, k, B, Hkv, N, d));
+  FA_TRY(tmap_bf16(&tv, v, B, Hkv, N, d));
+  fa::FwdArgs a;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.N = N;
+  a.causal = causal;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  return launch_status(fa::launch_fwd(d, tq, tk, tv, a, dev_status(ds), static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd_preprocess(const void* o, const void* dO, int B, int Hq, int Hkv, int N, int d, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!o || !dO || !workspace) return FA_ERR_NULL_PTR;
+  FA_TRY(check_shape(B, Hq, Hkv, N, d));
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(workspace)) return FA_ERR_MISALIGNED;
+  const WsLayout w = ws_layout(B, Hq, N, d);
+  if (workspace_bytes < w.total) return FA_ERR_WORKSPACE_TOO_SMALL;
+  const size_t qb = elems(B, Hq, N, d) * 2;
+  const Range rw = range(workspace, w.total);
+  if (overlap(rw, range(o, qb)) || overlap(rw, range(dO, qb))) return FA_ERR_ALIASING;
+  DeviceState* ds = nullptr;
+  FA_TRY(device_state(&ds));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return launch_status(fa::launch_bwd_preprocess(d, o, dO, reinterpret_cast<float*>(ws + w.dr_off),
+                                                 reinterpret_cast<float*>(ws + w.dq_off), (long long)B * Hq * N,
+                                                 ds->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse, void* dk,
+                      void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  FA_TRY(validate_dkdv(q, k, v, dO, lse, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
+  DeviceState* ds = nullptr;
+  FA_TRY(device_state(&ds));
+  CUtensorMap tq, tk, tv, tdo;
+  FA_TRY(tmap_bf16(&tq, q, B, Hq, N, d));
+  FA_TRY(tmap_bf16(&tk, k, B, Hkv, N, d));
+  FA_TRY(tmap_bf16(&tv, v, B, Hkv, N, d));
+  FA_TRY(tmap_bf16(&tdo, dO, B, Hq, N, d));
+  const WsLayout w = ws_layout(B, Hq, N, d);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  fa::BwdArgs a;
+  a.lse = lse;
+  a.drow = reinterpret_cast<const float*>(ws + w.dr_off);
+  a.dq_accum = reinterpret_cast<float*>(ws + w.dq_off);
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.N = N;
+  a.causal = causal;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  return launch_status(fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, a, dev_status(ds), static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd_dq_convert(void* dq, int B, int Hq, int Hkv, int N, int d, float scale, const void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!dq || !workspace) return FA_ERR_NULL_PTR;
+  FA_TRY(check_shape(B, Hq, Hkv, N, d));
+  FA_TRY(check_scale(0, scale));
+  if (!aligned16(dq) || !aligned16(workspace)) return FA_ERR_MISALIGNED;
+  const WsLayout w = ws_layout(B, Hq, N, d);
+  if (workspace_bytes < w.total) return FA_ERR_WORKSPACE_TOO_SMALL;
+  if (overlap(range(dq, elems(B, Hq, N, d) * 2), range(workspace, w.total))) return FA_ERR_ALIASING;
+  DeviceState* ds = nullptr;
+  FA_TRY(device_state(&ds));
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  return launch_status(fa::launch_bwd_dq_convert(reinterpret_cast<const float*>(ws + w.dq_off), dq, scale,
+                                                 (long long)elems(B, Hq, N, d), ds->num_sms,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (!o || !dq) return FA_ERR_NULL_PTR;
+  FA_TRY(validate_dkdv(q, k, v, dO, lse, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
+  if (!aligned16(o) || !aligned16(dq)) return FA_ERR_MISALIGNED;
+  const size_t qb = elems(B, Hq, N, d) * 2, kb = elems(B, Hkv, N, d) * 2;
+  const Range rdq = range(dq, qb);
+  const Range others[] = {range(q, qb),  range(k, kb),  range(v, kb),  range(o, qb), range(dO, qb),
+                          range(lse, (size_t)B * Hq * N * 4), range(dk, kb), range(dv, kb),
+                          range(workspace, ws_layout(B, Hq, N, d).total)};
+  for (const Range& r : others)
+    if (overlap(rdq, r)) return FA_ERR_ALIASING;
+  const Range ro = range(o, qb);
+  if (overlap(ro, range(dk, kb)) || overlap(ro, range(dv, kb)) ||
+      overlap(ro, range(workspace, ws_layout(B, Hq, N, d).total)))
+    return FA_ERR_ALIASING;
+  FA_TRY(fa_bwd_preprocess(o, dO, B, Hq, Hkv, N, d, workspace, workspace_bytes, stream));
+  FA_TRY(fa_bwd_dkdv(q, k, v, dO, lse, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, stream));
+  return fa_bwd_dq_convert(dq, B, Hq, Hkv, N, d, scale, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_last_device_status(void* stream, int* detail) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceState* ds = nullptr;
+  FA_TRY(device_state(&ds));
+  int words[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(words, ds->status, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  const int zero[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(ds->status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  if (detail) {
+    detail[0] = words[1];
+    detail[1] = words[2];
+    detail[2] = words[3];
+  }
+  return static_cast<fa_status>(words[0]);
+}
+
+fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) {
+  if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return FA_ERR_BAD_ARGUMENT;
+  DeviceState* ds = nullptr;
+  FA_TRY(device_state(&ds));
+  fa::DevStatus st{ds->status, timeout_ns};
+  wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st);
+  return launch_status(cudaGetLastError());
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// Internal launcher interface between the C-ABI layer (fa_api.cu) and the
+// kernels.  Nothing here is exported from the shared library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "sm103a.cuh"
+
+namespace fa {
+
+struct FwdArgs {
+  void* o;            // [B, Hq, N, d] bf16
+  float* lse;         // [B, Hq, N] fp32, natural log
+  int B, Hq, Hkv, N;
+  int causal;
+  float scale_log2;   // scale * log2(e)
+};
+
+struct BwdArgs {
+  const void* lse;    // [B, Hq, N] fp32 (natural log, from the forward)
+  const float* drow;  // [B, Hq, N] fp32, rowsum(dO * O) (workspace)
+  float* dq_accum;    // [B, Hq, N, d] fp32 (workspace)
+  void* dk;           // [B, Hkv, N, d] bf16
+  void* dv;           // [B, Hkv, N, d] bf16
+  int B, Hq, Hkv, N;
+  int causal;
+  float scale;        // softmax scale
+  float scale_log2;   // scale * log2(e)
+};
+
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+                       const DevStatus& st, cudaStream_t stream);
+
+cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dO, float* drow, float* dq_accum, long long rows,
+                                  int num_sms, cudaStream_t stream);
+
+cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, const DevStatus& st, cudaStream_t stream);
+
+cudaError_t launch_bwd_dq_convert(const float* dq_accum, void* dq, float scale, long long n, int num_sms,
+                                  cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(const DevStatus& st, cudaStream_t stream);
+
+}  // namespace fa

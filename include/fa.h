@@ -1,0 +1,135 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library, libfa_gb300.so.
+ *
+ * What is computed (exact scaled-dot-product self-attention):
+ *   For batch b and query head h, with key/value head g = h / (Hq / Hkv),
+ *     S = scale * Q[b,h] K[b,g]^T,  P = softmax(S) per row,  O[b,h] = P V[b,g],
+ *     LSE[b,h,i] = ln sum_j exp(S[i,j])   (natural log, scale included).
+ *   Causal: query i sees key j iff j <= i.
+ *   Pages: [QBank-36] "十九、分布式与系统方向的标准答案速查区", question #36
+ *   ("FlashAttention 为什么常被说成是 IO-aware 优化"), parts 2-3 (S = QK^T,
+ *   P = softmax(S), O = PV over B x H x L x d tensors; tiling with an online
+ *   softmax, S and P never written to HBM); [Lecture] Stanford lecture
+ *   summary, "推导 FlashAttention 的在线 softmax" (running max and
+ *   numerator/denominator rescaled by exp(old - new); the backward pass
+ *   recomputes from small saved statistics), "GPU 显存和注意力瓶颈" (causal
+ *   self-attention) and "减少缓存表示并验证草稿" (Hq query heads sharing
+ *   Hkv key/value groups: Hkv == Hq is multi-head, Hkv == 1 multi-query).
+ *   The result is exact up to floating-point rounding: bf16 inputs, fp32
+ *   accumulation, bf16 outputs (round to nearest even), fp32 LSE.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are DEVICE pointers to contiguous row-major arrays:
+ *       q, o, dO, dq : bf16 [B, Hq,  N, d]     (d innermost)
+ *       k, v, dk, dv : bf16 [B, Hkv, N, d]
+ *       lse          : fp32 [B, Hq,  N]
+ *   - Every pointer must be 16-byte aligned (FA_ERR_MISALIGNED otherwise).
+ *   - d must be 64 or 128 (FA_ERR_UNSUPPORTED_HEADDIM otherwise);
+ *     B, Hq, Hkv, N >= 1, Hq % Hkv == 0, B <= 65535 and N <= 8388480
+ *     (65535 tiles of 128 rows) (FA_ERR_BAD_SHAPE otherwise).
+ *   - scale must be finite and > 0 (FA_ERR_BAD_ARGUMENT otherwise).
+ *   - Outputs must not overlap any input or each other (FA_ERR_ALIASING).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued on it and the call returns without synchronising.  The library
+ *     never allocates or frees memory; the caller owns every buffer.
+ *   - Errors are returned as fa_status; nothing aborts or prints.  Argument
+ *     checks happen before any CUDA call, so an invalid call enqueues nothing.
+ *   - Requires a compute capability 10.3 (GB300) device current on the
+ *     calling thread (FA_ERR_UNSUPPORTED_DEVICE otherwise).
+ *   - Every device-side wait is bounded: if a kernel's internal wait runs out
+ *     (it should not), the kernel stops, leaves its outputs incomplete and
+ *     records FA_ERR_DEVICE_TIMEOUT, which fa_last_device_status() reports.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_NULL_PTR = 1,             /* a required pointer is NULL */
+  FA_ERR_BAD_SHAPE = 2,            /* B, Hq, Hkv, N < 1, Hq % Hkv != 0, or too large */
+  FA_ERR_UNSUPPORTED_HEADDIM = 3,  /* d not in {64, 128} */
+  FA_ERR_MISALIGNED = 4,           /* a pointer is not 16-byte aligned */
+  FA_ERR_WORKSPACE_TOO_SMALL = 5,  /* workspace_bytes < fa_bwd_workspace_bytes(...) */
+  FA_ERR_UNSUPPORTED_DEVICE = 6,   /* current device is not sm_103 */
+  FA_ERR_LAUNCH = 7,               /* a kernel launch or tensor-map encode failed */
+  FA_ERR_DEVICE_TIMEOUT = 8,       /* a device-side bounded wait ran out */
+  FA_ERR_CUDA = 9,                 /* another CUDA runtime error */
+  FA_ERR_BAD_ARGUMENT = 10,        /* scale not finite / not > 0, causal not 0/1 */
+  FA_ERR_ALIASING = 11             /* an output overlaps an input or another output */
+} fa_status;
+
+/*
+ * Forward pass.  Writes o [B,Hq,N,d] bf16 and lse [B,Hq,N] fp32.
+ * q, k, v are read only.  One kernel launch.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                 int d, int causal, float scale, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: the fp32 dQ accumulator
+ * [B,Hq,N,d] followed by the fp32 row term D = rowsum(dO * O) [B,Hq,N], each
+ * rounded up to 256 bytes.  Returns 0 for invalid shapes.  O(N * d) per head:
+ * no N x N buffer.
+ */
+size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
+
+/*
+ * Backward pass: given q, k, v, the forward's o and lse, and dO, writes
+ * dq [B,Hq,N,d], dk and dv [B,Hkv,N,d] (bf16), the gradients of
+ * sum(dO * O).  P is recomputed tile by tile from lse; no N x N buffer.
+ * `workspace` (device, >= fa_bwd_workspace_bytes) is scratch owned by the
+ * caller; its contents on entry do not matter.  Equivalent to
+ * fa_bwd_preprocess + fa_bwd_dkdv + fa_bwd_dq_convert in that order.
+ * dq is not bitwise reproducible run to run: the fp32 dQ accumulation order
+ * across key tiles is not fixed.  dk and dv are (one owner per key tile).
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward step 1: D = rowsum(dO * O) into the workspace; zero the dQ accumulator. */
+fa_status fa_bwd_preprocess(const void* o, const void* dO, int B, int Hq, int Hkv, int N, int d, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Backward step 2: dk, dv (written) and the dQ accumulator (added into). Needs step 1. */
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse, void* dk,
+                      void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Backward step 3: dq = bf16(scale * dQ accumulator). Needs step 2. */
+fa_status fa_bwd_dq_convert(void* dq, int B, int Hq, int Hkv, int N, int d, float scale, const void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Static text for a status code (never NULL). */
+const char* fa_strerror(fa_status status);
+
+/*
+ * Synchronises `stream`, then returns and clears the first device-side error
+ * any kernel of this library recorded on the current device (FA_OK if none),
+ * or FA_ERR_CUDA if the synchronisation itself failed.  If `detail` is not
+ * NULL it receives 3 ints: flattened block index, wait-site id, thread index.
+ */
+fa_status fa_last_device_status(void* stream, int* detail);
+
+/*
+ * Self-test of the bounded-wait mechanism: launches one CTA that waits on a
+ * barrier nothing will complete, with a limit of `timeout_ns` nanoseconds
+ * (1e3 .. 1e10).  Afterwards fa_last_device_status() must report
+ * FA_ERR_DEVICE_TIMEOUT and the device stays usable.  No fault is involved.
+ */
+fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
+/* Library ABI version (major * 100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

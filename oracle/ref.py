@@ -78,19 +78,34 @@ def _rows_of_p(q_blk, k_g, rows, N, causal, scale):
     return softmax_rows(s)
 
 
-def attention_forward(q, k, v, causal: bool, scale: float, row_block: int = 512):
-    """O [B,Hq,N,d] and LSE [B,Hq,N] of exact attention, in fp64."""
+def _row_span(N, row_range):
+    if row_range is None:
+        return 0, N
+    r0, r1 = row_range
+    if not (0 <= r0 <= r1 <= N):
+        raise ValueError("row_range outside [0, N]")
+    return r0, r1
+
+
+def attention_forward(q, k, v, causal: bool, scale: float, row_block: int = 512, row_range=None):
+    """O [B,Hq,N,d] and LSE [B,Hq,N] of exact attention, in fp64.
+
+    ``row_range=(r0, r1)`` computes only query rows r0..r1-1 (the other rows of
+    the outputs are left as NaN); each row is still the full two-pass softmax
+    over every key, so a row range is a bounded sample of the same work.
+    """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     B, Hq, Hkv, N, d = _check_shapes(q, k, v)
-    o = np.empty((B, Hq, N, d))
-    lse = np.empty((B, Hq, N))
+    lo, hi = _row_span(N, row_range)
+    o = np.full((B, Hq, N, d), np.nan)
+    lse = np.full((B, Hq, N), np.nan)
     for b in range(B):
         for h in range(Hq):
             g = kv_head_index(h, Hq, Hkv)
-            for r0 in range(0, N, row_block):
-                r1 = min(N, r0 + row_block)
+            for r0 in range(lo, hi, row_block):
+                r1 = min(hi, r0 + row_block)
                 rows = np.arange(r0, r1)
                 p, m, den = _rows_of_p(q[b, h, r0:r1], k[b, g], rows, N, causal, scale)
                 o[b, h, r0:r1] = p @ v[b, g]
@@ -98,8 +113,12 @@ def attention_forward(q, k, v, causal: bool, scale: float, row_block: int = 512)
     return o, lse
 
 
-def attention_backward(q, k, v, do, causal: bool, scale: float, row_block: int = 512):
-    """(dQ, dK, dV) of L = sum(dO * O) for exact attention, in fp64."""
+def attention_backward(q, k, v, do, causal: bool, scale: float, row_block: int = 512, row_range=None):
+    """(dQ, dK, dV) of L = sum(dO * O) for exact attention, in fp64.
+
+    ``row_range=(r0, r1)`` restricts the sum to query rows r0..r1-1: dQ rows
+    outside it are zero and dK/dV hold only those rows' contributions.
+    """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -110,11 +129,12 @@ def attention_backward(q, k, v, do, causal: bool, scale: float, row_block: int =
     dq = np.zeros((B, Hq, N, d))
     dk = np.zeros((B, Hkv, N, d))
     dv = np.zeros((B, Hkv, N, d))
+    lo, hi = _row_span(N, row_range)
     for b in range(B):
         for h in range(Hq):
             g = kv_head_index(h, Hq, Hkv)
-            for r0 in range(0, N, row_block):
-                r1 = min(N, r0 + row_block)
+            for r0 in range(lo, hi, row_block):
+                r1 = min(hi, r0 + row_block)
                 rows = np.arange(r0, r1)
                 q_blk = q[b, h, r0:r1]
                 do_blk = do[b, h, r0:r1]

@@ -438,3 +438,20 @@ def test_mutant_off_by_one_causal_is_caught(monkeypatch):
                         else np.ones((len(rows), N), bool))
     with np.errstate(all="ignore"):
         assert not run_pin(pin_causal_row0, ref.attention_forward, ref.attention_backward)
+
+
+def test_row_range_is_a_partition():
+    # Row ranges split the rows exactly: forward rows agree, and the dK/dV
+    # contributions of disjoint ranges add up to the full gradients.
+    q, k, v, do = (rand((1, 2, 40, 4), s) for s in (100, 101, 102, 103))
+    for causal in (False, True):
+        o, l = ref.attention_forward(q, k, v, causal, 0.5)
+        oa, la = ref.attention_forward(q, k, v, causal, 0.5, row_range=(0, 13))
+        ob, lb = ref.attention_forward(q, k, v, causal, 0.5, row_range=(13, 40))
+        assert np.allclose(o[:, :, :13], oa[:, :, :13], atol=1e-14) and np.isnan(oa[:, :, 13:]).all()
+        assert np.allclose(l[:, :, 13:], lb[:, :, 13:], atol=1e-14)
+        full = ref.attention_backward(q, k, v, do, causal, 0.5)
+        pa = ref.attention_backward(q, k, v, do, causal, 0.5, row_range=(0, 13))
+        pb = ref.attention_backward(q, k, v, do, causal, 0.5, row_range=(13, 40))
+        for f, a, b in zip(full, pa, pb):
+            assert np.allclose(f, a + b, atol=1e-13)
