@@ -45,6 +45,22 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank float over the default process group (identity if none)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(step_flops: float, world: int, total_ms_max: float, steps: int) -> float:
+    """Whole-job TFLOPS: the work of every rank over the slowest rank's time."""
+    return step_flops * world * steps / (total_ms_max * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------------------
 # measured peaks, kernel source hash, ncu traffic record
 # ---------------------------------------------------------------------------
@@ -315,14 +331,10 @@ def run_ours(args, w):
     dkdv_ms = [e[2].elapsed_time(e[3]) for e in events]
     conv_ms = [e[3].elapsed_time(e[4]) for e in events]
     step_ms = [e[0].elapsed_time(e[4]) for e in events]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
     step_flops = w.fwd_flops + w.bwd_flops
-    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+    value = aggregate_tflops(step_flops, world, total_ms, args.steps)
 
     peak, peak_src = bf16_peak()
     fwd_avg = statistics.mean(fwd_ms)
