@@ -36,6 +36,8 @@ FA_ERR_DEVICE_TIMEOUT = 8
 FA_ERR_CUDA = 9
 FA_ERR_BAD_ARGUMENT = 10
 FA_ERR_ALIASING = 11
+FA_ERR_SCRATCH_LIMIT = 12
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 class FAError(RuntimeError):
@@ -63,6 +65,7 @@ _SIGNATURES = {
     "fa_last_device_status": ([_p, ctypes.POINTER(ctypes.c_int)], _i),
     "fa_selftest_wait_timeout": ([ctypes.c_ulonglong, _p], _i),
     "fa_version": ([], _i),
+    "fa_bwd_noalloc": ([_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p], _i),
 }
 
 
@@ -144,6 +147,13 @@ def fa_selftest_wait_timeout(timeout_ns, stream=None):
 
 def fa_version():
     return load_library().fa_version()
+
+
+def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, stream):
+    """fa_bwd without a workspace argument: the scratch is a fixed buffer inside
+    the library (for callers that cannot allocate device memory)."""
+    return load_library().fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, int(causal),
+                                         float(scale), stream)
 
 
 # ---------------------------------------------------------------------------

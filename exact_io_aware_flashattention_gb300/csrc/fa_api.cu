@@ -187,6 +187,8 @@ const char* fa_strerror(fa_status s) {
     case FA_ERR_CUDA: return "CUDA runtime error";
     case FA_ERR_BAD_ARGUMENT: return "bad argument (scale must be finite and > 0, causal 0 or 1)";
     case FA_ERR_ALIASING: return "an output overlaps an input or another output";
+    case FA_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than fa_bwd_noalloc's built-in buffer (FA_NOALLOC_SCRATCH_BYTES) holds";
   }
   return "unknown status";
 }
@@ -339,3 +341,53 @@ fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// fa_bwd_noalloc: fa_bwd with its scratch in a buffer compiled into the
+// library, for callers that cannot allocate device memory.
+// ---------------------------------------------------------------------------
+namespace {
+
+// The scratch lives here, in the library's own device image: every device
+// that loads the library holds these FA_NOALLOC_SCRATCH_BYTES until exit.
+// In host code this name is only a stand-in for the symbol, not a device
+// address; the address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device, looked up once per
+// device with that device current.
+fa_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                    const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                                    int d, int causal, float scale, void* stream) {
+  FA_TRY(check_shape(B, Hq, Hkv, N, d));
+  if (ws_layout(B, Hq, N, d).total > (size_t)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL_PTR;
+  FA_TRY(check_scale(causal, scale));
+  DeviceState* ds = nullptr;
+  FA_TRY(device_state(&ds));
+  void* scratch = nullptr;
+  FA_TRY(noalloc_scratch(&scratch));
+  // fa_bwd clears the dQ accumulator in its first kernel, so whatever the
+  // previous call left in the scratch does not matter.
+  return fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, scratch,
+                (size_t)FA_NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -61,7 +61,8 @@ typedef enum fa_status {
   FA_ERR_DEVICE_TIMEOUT = 8,       /* a device-side bounded wait ran out */
   FA_ERR_CUDA = 9,                 /* another CUDA runtime error */
   FA_ERR_BAD_ARGUMENT = 10,        /* scale not finite / not > 0, causal not 0/1 */
-  FA_ERR_ALIASING = 11             /* an output overlaps an input or another output */
+  FA_ERR_ALIASING = 11,            /* an output overlaps an input or another output */
+  FA_ERR_SCRATCH_LIMIT = 12        /* fa_bwd_noalloc: problem needs more than FA_NOALLOC_SCRATCH_BYTES */
 } fa_status;
 
 /*
@@ -124,6 +125,35 @@ fa_status fa_last_device_status(void* stream, int* detail);
  * FA_ERR_DEVICE_TIMEOUT and the device stays usable.  No fault is involved.
  */
 fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
+/*
+ * Backward pass for callers that must not allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot hand fa_bwd a workspace: code that runs under a memory manager
+ * owning every byte of the device (a framework's caching pool, an inference
+ * runtime with a fixed arena), hosts whose plugins are not allowed to call
+ * cudaMalloc/cudaFree at run time, and hot paths where cudaMalloc is too
+ * costly or would synchronise the device.
+ *
+ * Same arguments, layout and result as fa_bwd, without the workspace: the
+ * scratch (fp32 dQ accumulator and row term, fa_bwd_workspace_bytes() bytes)
+ * lives in a fixed FA_NOALLOC_SCRATCH_BYTES buffer compiled into this
+ * library.  Every GPU that loads the library keeps that buffer until the
+ * process exits.  The call allocates and frees nothing.
+ *   - Problems whose fa_bwd_workspace_bytes() exceeds the buffer are rejected
+ *     with FA_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *   - The first call on a device looks the buffer's device address up once
+ *     (with that device current); make that first call before any stream
+ *     capture begins.
+ *   - All calls on a device share the one buffer and each starts by clearing
+ *     what must start at zero.  Calls whose kernels overlap on the GPU (other
+ *     streams, or other threads) race on it: serialise them.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
+                         int causal, float scale, void* stream);
 
 /* Library ABI version (major * 100 + minor). */
 int fa_version(void);

@@ -33,7 +33,7 @@ def test_binding_exposes_same_names():
 
 def test_version_and_strerror(lib):
     assert fa.fa_version() == 100
-    for code in range(0, 12):
+    for code in range(0, 13):
         assert fa.fa_strerror(code)
     assert fa.fa_strerror(999) == "unknown status"
 
