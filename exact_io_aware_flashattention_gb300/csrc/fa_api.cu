@@ -94,6 +94,7 @@ fa_status check_shape(int B, int Hq, int Hkv, int N, int d) {
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return FA_ERR_BAD_SHAPE;
   if (Hq % Hkv != 0) return FA_ERR_BAD_SHAPE;
   if (B > 65535 || N > 65535 * 128) return FA_ERR_BAD_SHAPE;
+  if ((long long)((N + 127) / 128) * Hq * B >= (1LL << 31)) return FA_ERR_BAD_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_HEADDIM;
   return FA_OK;
 }
@@ -177,7 +178,9 @@ const char* fa_strerror(fa_status s) {
   switch (s) {
     case FA_OK: return "ok";
     case FA_ERR_NULL_PTR: return "a required pointer is NULL";
-    case FA_ERR_BAD_SHAPE: return "bad shape (B, Hq, Hkv, N must be >= 1, Hq % Hkv == 0, B <= 65535, N <= 8388480)";
+    case FA_ERR_BAD_SHAPE:
+      return "bad shape (B, Hq, Hkv, N must be >= 1, Hq % Hkv == 0, B <= 65535, N <= 8388480, "
+             "ceil(N/128)*Hq*B < 2^31)";
     case FA_ERR_UNSUPPORTED_HEADDIM: return "unsupported head dimension (d must be 64 or 128)";
     case FA_ERR_MISALIGNED: return "a pointer is not 16-byte aligned";
     case FA_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than fa_bwd_workspace_bytes()";
@@ -226,7 +229,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   a.N = N;
   a.causal = causal;
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_status(fa::launch_fwd(d, tq, tk, tv, a, dev_status(ds), static_cast<cudaStream_t>(stream)));
+  return launch_status(
+      fa::launch_fwd(d, tq, tk, tv, a, dev_status(ds), ds->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_bwd_preprocess(const void* o, const void* dO, int B, int Hq, int Hkv, int N, int d, void* workspace,

@@ -7,16 +7,25 @@
 // tensor memory, update a running row max m and running denominator l,
 // rescale the running output by exp(m_old - m_new) when the max grows, and
 // accumulate P V.  O / l and LSE = m + ln l are written once at the end.
+// Multiplying numerator and denominator by one factor leaves their ratio
+// unchanged ([Lecture], same section), so the reference max may lag the true
+// max: it is only raised when the true max exceeds it by more than 2^8 (log2
+// units), which keeps every exponent <= 2^8 and skips most rescales.
 //
-// CTA layout (192 threads, one CTA per SM):
-//   warp 0     TMA producer: Q tile once, then K_j / V_j into a 2-stage ring
+// Persistent kernel: one CTA per SM walks work items (query tile, head,
+// batch), heaviest causal tiles first.  CTA layout (224 threads):
+//   warp 0     TMA producer for Q (2 slots) and K (ring of kStagesK)
 //   warp 1     TMEM allocator and tcgen05.mma issuer (one elected thread)
-//   warps 2-5  softmax warpgroup: thread t of the group owns query row t of
-//              the tile (TMEM lane t), so row max / row sum are in-thread
-// Tensor memory (512 columns): S double buffer at columns 0 and 128
-// (fp32 128 x 128 each), O accumulator at column 256 (fp32 128 x d).
-// P (bf16, 128 x 128) goes through a shared-memory tile as the A operand of
-// the P V MMA.
+//   warps 2-5  softmax warpgroup: thread t owns query row t of the tile (TMEM
+//              lane t), so row max and row sum are in-thread reductions
+//   warp 6     TMA producer for V (ring of kStagesV)
+// Tensor memory (512 columns): three fp32 128x128 score buffers at columns
+// 0, 128, 256; the O accumulator (fp32 128 x d) at 384.  P (bf16) is written
+// over the first 64 columns of its own score buffer and read from there by
+// the P V MMA, so P never touches shared memory.  With three buffers the
+// tensor pipe computes S two tiles ahead of P V:
+//   S0 S1 | PV0 S2 | PV1 S3 | PV2 S4 ...
+// and the softmax of tile t has the two MMAs before PV_t to finish.
 #include "fa_internal.h"
 #include "sm103a.cuh"
 
@@ -24,47 +33,95 @@ namespace fa {
 
 namespace {
 
-constexpr int kBM = 128;       // query rows per tile
-constexpr int kBN = 128;       // keys per tile
-constexpr int kStages = 2;     // K/V ring depth
-constexpr int kThreads = 192;
+constexpr int kBM = 128;        // query rows per tile
+constexpr int kBN = 128;        // keys per tile
+constexpr int kSBuf = 3;        // score / probability buffers in tensor memory
+constexpr int kThreads = 224;
 constexpr uint32_t kBlockBytes = 128u * 128u;   // one 64-column block of a 128-row bf16 tile
+constexpr float kRescaleThreshold = 8.0f;
 
 template <int D>
-struct FwdSmem {
+struct FwdCfg {
+  static constexpr int kStagesK = D == 128 ? 3 : 4;
+  static constexpr int kStagesV = D == 128 ? 2 : 4;
   static constexpr uint32_t kTile = 128u * D * 2u;
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kTile;
-  static constexpr uint32_t kV = kK + kStages * kTile;
-  static constexpr uint32_t kP = kV + kStages * kTile;
-  static constexpr uint32_t kBar = kP + 128u * 128u * 2u;
-  static constexpr uint32_t kBytes = kBar + 256u;
-  static constexpr uint32_t kAlloc = kBytes + 1024u;   // slack for 1024-byte alignment
+  static constexpr uint32_t kQ = 0;                              // 2 slots
+  static constexpr uint32_t kK = kQ + 2u * kTile;
+  static constexpr uint32_t kV = kK + kStagesK * kTile;
+  static constexpr uint32_t kBar = kV + kStagesV * kTile;
+  static constexpr uint32_t kBytes = kBar + 512u;
+  static constexpr uint32_t kAlloc = kBytes + 1024u;            // slack for 1024-byte alignment
 };
 
 // Wait-site ids reported in the status words.
-enum : int { kSiteQ = 1, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSitePFull, kSiteVFull, kSiteSFull, kSiteODone };
+enum : int {
+  kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSitePFull, kSiteVFull, kSiteOFree,
+  kSiteOPrev, kSiteSFull, kSiteORescale, kSiteOLast
+};
 
 struct Bars {
-  uint64_t q_full;
-  uint64_t k_full[kStages];
-  uint64_t v_full[kStages];
-  uint64_t k_empty[kStages];
-  uint64_t v_empty[kStages];
-  uint64_t s_full[2];
-  uint64_t p_full;
-  uint64_t o_done;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[4], k_empty[4];
+  uint64_t v_full[4], v_empty[4];
+  uint64_t s_full[kSBuf], p_full[kSBuf];
+  uint64_t o_done[2];
+  uint64_t o_free;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+};
+
+struct Item {
+  int qt, h, b, kvh, n;
+};
+
+// Work items are ordered heaviest first: rank r covers query tile nt-1-r of
+// every (head, batch) when causal (tile r otherwise).
+__device__ __forceinline__ Item decode_item(int idx, const FwdArgs& a, int nt) {
+  const int per = a.Hq * a.B;
+  const int rank = idx / per;
+  const int hb = idx - rank * per;
+  Item it;
+  it.qt = a.causal ? nt - 1 - rank : rank;
+  it.h = hb % a.Hq;
+  it.b = hb / a.Hq;
+  it.kvh = it.h / (a.Hq / a.Hkv);
+  it.n = a.causal ? min(it.qt + 1, nt) : nt;
+  return it;
+}
+
+// Walks this CTA's (item, key tile) sequence.
+struct Cursor {
+  int item, li, j, n_items, nt;
+  Item it;
+  bool valid;
+  __device__ __forceinline__ void init(const FwdArgs& a, int nt_, int n_items_) {
+    nt = nt_;
+    n_items = n_items_;
+    item = blockIdx.x;
+    li = 0;
+    j = 0;
+    valid = item < n_items;
+    if (valid) it = decode_item(item, a, nt);
+  }
+  __device__ __forceinline__ void next(const FwdArgs& a) {
+    if (++j == it.n) {
+      j = 0;
+      item += gridDim.x;
+      ++li;
+      valid = item < n_items;
+      if (valid) it = decode_item(item, a, nt);
+    }
+  }
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args, const DevStatus st) {
-  using L = FwdSmem<D>;
+  using L = FwdCfg<D>;
   constexpr int kAtoms = D / 64;
+  constexpr int SK = L::kStagesK, SV = L::kStagesV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBar);
@@ -72,26 +129,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.x;
-  const int b = blockIdx.y;
   const int N = args.N;
   const int nt = (N + kBM - 1) / kBM;
-  const int qt = args.causal ? (nt - 1 - (int)blockIdx.z) : (int)blockIdx.z;
-  const int kvh = h / (args.Hq / args.Hkv);
-  const int n_kv = args.causal ? min(qt + 1, nt) : nt;
+  const int n_items = nt * args.Hq * args.B;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+      mbar_init(&bars->o_done[i], 1);
+    }
+    for (int s = 0; s < SK; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < SV; ++s) {
+      mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    mbar_init(&bars->s_full[0], 1);
-    mbar_init(&bars->s_full[1], 1);
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->o_done, 1);
+    for (int s = 0; s < kSBuf; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->p_full[s], 128);
+    }
+    mbar_init(&bars->o_free, 128);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     mbar_fence_init();
@@ -108,195 +168,273 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
+  const uint32_t tO = tmem + 384;
 
   const uint32_t sQ = smem_u32(smem + L::kQ);
   const uint32_t sK = smem_u32(smem + L::kK);
   const uint32_t sV = smem_u32(smem + L::kV);
-  const uint32_t sP = smem_u32(smem + L::kP);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------ Q / K producer
     if (lane == 0) {
-      int k_issued[kStages] = {0, 0}, v_issued[kStages] = {0, 0};
-      mbar_arrive_expect_tx(&bars->q_full, L::kTile);
-      for (int a = 0; a < kAtoms; ++a)
-        tma_load_4d(smem + L::kQ + a * kBlockBytes, &tmQ, &bars->q_full, a * 64, qt * kBM, h, b);
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % kStages, r = j / kStages;
-        if (r > 0 && !mbar_wait(&bars->k_empty[s], (r - 1) & 1, st, abort_flag, kSiteKEmpty)) break;
-        mbar_arrive_expect_tx(&bars->k_full[s], L::kTile);
+      int kt = 0, li = 0;
+      int q_issued[2] = {0, 0};
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++li) {
+        const Item it = decode_item(item, args, nt);
+        const int slot = li & 1;
+        if (li >= 2 && !mbar_wait(&bars->q_empty[slot], ((li >> 1) - 1) & 1, st, abort_flag, kSiteQEmpty)) break;
+        mbar_arrive_expect_tx(&bars->q_full[slot], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
-          tma_load_4d(smem + L::kK + s * L::kTile + a * kBlockBytes, &tmK, &bars->k_full[s], a * 64, j * kBN,
-                      kvh, b);
-        ++k_issued[s];
-        if (r > 0 && !mbar_wait(&bars->v_empty[s], (r - 1) & 1, st, abort_flag, kSiteVEmpty)) break;
-        mbar_arrive_expect_tx(&bars->v_full[s], L::kTile);
-        for (int a = 0; a < kAtoms; ++a)
-          tma_load_4d(smem + L::kV + s * L::kTile + a * kBlockBytes, &tmV, &bars->v_full[s], a * 64, j * kBN,
-                      kvh, b);
-        ++v_issued[s];
+          tma_load_4d(smem + L::kQ + slot * L::kTile + a * kBlockBytes, &tmQ, &bars->q_full[slot], a * 64,
+                      it.qt * kBM, it.h, it.b);
+        ++q_issued[slot];
+        for (int j = 0; j < it.n; ++j, ++kt) {
+          const int s = kt % SK, r = kt / SK;
+          if (r > 0 && !mbar_wait(&bars->k_empty[s], (r - 1) & 1, st, abort_flag, kSiteKEmpty)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->k_full[s], L::kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_4d(smem + L::kK + s * L::kTile + a * kBlockBytes, &tmK, &bars->k_full[s], a * 64, j * kBN,
+                        it.kvh, it.b);
+        }
       }
       // Every copy issued must have landed before the CTA may exit.
-      mbar_wait_drain(&bars->q_full, 0, st.timeout_ns);
-      for (int s = 0; s < kStages; ++s) {
-        if (k_issued[s]) mbar_wait_drain(&bars->k_full[s], (k_issued[s] - 1) & 1, st.timeout_ns);
-        if (v_issued[s]) mbar_wait_drain(&bars->v_full[s], (v_issued[s] - 1) & 1, st.timeout_ns);
+      for (int i = 0; i < 2; ++i)
+        if (q_issued[i]) mbar_wait_drain(&bars->q_full[i], (q_issued[i] - 1) & 1, st.timeout_ns);
+      for (int s = 0; s < SK && s < kt; ++s) {
+        const int last = kt - 1 - ((kt - 1 - s) % SK);   // last tile issued into stage s
+        mbar_wait_drain(&bars->k_full[s], (last / SK) & 1, st.timeout_ns);
+      }
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------ V producer
+    if (lane == 0) {
+      int vt = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const Item it = decode_item(item, args, nt);
+        for (int j = 0; j < it.n; ++j, ++vt) {
+          const int s = vt % SV, r = vt / SV;
+          if (r > 0 && !mbar_wait(&bars->v_empty[s], (r - 1) & 1, st, abort_flag, kSiteVEmpty)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->v_full[s], L::kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_4d(smem + L::kV + s * L::kTile + a * kBlockBytes, &tmV, &bars->v_full[s], a * 64, j * kBN,
+                        it.kvh, it.b);
+        }
+      }
+      for (int s = 0; s < SV && s < vt; ++s) {
+        const int last = vt - 1 - ((vt - 1 - s) % SV);
+        mbar_wait_drain(&bars->v_full[s], (last / SV) & 1, st.timeout_ns);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
       constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
-      bool ok = mbar_wait(&bars->q_full, 0, st, abort_flag, kSiteQ);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % kStages;
-        if (!mbar_wait(&bars->k_full[s], (j / kStages) & 1, st, abort_flag, kSiteKFull)) return false;
+      Cursor sc;
+      sc.init(args, nt, n_items);
+      int ts = 0;   // global index of the next score tile to issue
+      // S_ts = Q K^T into buffer ts % 3.  The caller guarantees the buffer's
+      // previous P has been consumed.
+      auto issue_s = [&]() -> bool {
+        if (!sc.valid) return true;
+        const int buf = ts % kSBuf;
+        if (sc.j == 0 &&
+            !mbar_wait(&bars->q_full[sc.li & 1], (sc.li >> 1) & 1, st, abort_flag, kSiteQFull))
+          return false;
+        const int s = ts % SK;
+        if (!mbar_wait(&bars->k_full[s], (ts / SK) & 1, st, abort_flag, kSiteKFull)) return false;
         tc_fence_after();
-        const uint32_t kt = sK + s * L::kTile;
-        const uint32_t dS = (j & 1) ? tS1 : tS0;
+        const uint32_t qa = sQ + (sc.li & 1) * L::kTile;
+        const uint32_t ka = sK + s * L::kTile;
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
-          mma_bf16_ss(dS, desc_kmajor(sQ, k16, kBlockBytes), desc_kmajor(kt, k16, kBlockBytes), idS, k16 > 0);
-        mma_commit(&bars->s_full[j & 1]);
+          mma_bf16_ss(tmem + buf * 128, desc_kmajor(qa, k16, kBlockBytes), desc_kmajor(ka, k16, kBlockBytes), idS,
+                      k16 > 0);
+        mma_commit(&bars->s_full[buf]);
         mma_commit(&bars->k_empty[s]);
+        if (sc.j == sc.it.n - 1) mma_commit(&bars->q_empty[sc.li & 1]);
+        ++ts;
+        sc.next(args);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv && !issue_s(j + 1)) break;
-        if (!mbar_wait(&bars->p_full, j & 1, st, abort_flag, kSitePFull)) break;
+      bool ok = issue_s() && issue_s();
+      Cursor pc;
+      pc.init(args, nt, n_items);
+      for (int t = 0; ok && pc.valid; ++t, pc.next(args)) {
+        const int buf = t % kSBuf;
+        if (!mbar_wait(&bars->p_full[buf], (t / kSBuf) & 1, st, abort_flag, kSitePFull)) break;
+        const int v = t % SV;
+        if (!mbar_wait(&bars->v_full[v], (t / SV) & 1, st, abort_flag, kSiteVFull)) break;
+        if (pc.j == 0 && pc.li > 0 && !mbar_wait(&bars->o_free, (pc.li - 1) & 1, st, abort_flag, kSiteOFree)) break;
         tc_fence_after();
-        const int s = j % kStages;
-        if (!mbar_wait(&bars->v_full[s], (j / kStages) & 1, st, abort_flag, kSiteVFull)) break;
-        tc_fence_after();
-        const uint32_t vt = sV + s * L::kTile;
+        const uint32_t va = sV + v * L::kTile;
 #pragma unroll
         for (int k16 = 0; k16 < kBN / 16; ++k16)
-          mma_bf16_ss(tO, desc_kmajor(sP, k16, kBlockBytes), desc_mnmajor(vt, k16, kBlockBytes), idO,
-                      (j > 0 || k16 > 0) ? 1u : 0u);
-        mma_commit(&bars->o_done);
-        mma_commit(&bars->v_empty[s]);
+          mma_bf16_ts(tO, tmem + buf * 128 + k16 * 8, desc_mnmajor(va, k16, kBlockBytes), idO,
+                      (pc.j > 0 || k16 > 0) ? 1u : 0u);
+        mma_commit(&bars->o_done[t & 1]);
+        mma_commit(&bars->v_empty[v]);
+        // S_{t+2} goes into the buffer that held P_{t-1}: P V_{t-1} must be done.
+        if (t >= 1 && !mbar_wait(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteOPrev))
+          break;
+        tc_fence_after();
+        if (!issue_s()) break;
       }
       // No MMA may still be writing tensor memory when it is freed.
       mma_commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, st.timeout_ns);
     }
   } else {
-    // ------------------------------------------------------------ softmax
+    // ------------------------------------------------------ softmax
     const int quad = warp & 3;
     const int r = quad * 32 + lane;              // row within the tile == TMEM lane
-    const int row = qt * kBM + r;                // query index
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float sl2 = args.scale_log2;
-    float m_run = -INFINITY;                     // running max of scale*log2(e)*s
-    float l_run = 0.f;                           // running denominator
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!mbar_wait_warp(&bars->s_full[j & 1], (j >> 1) & 1, st, abort_flag, kSiteSFull)) { ok = false; break; }
+    const uint64_t sl2x2 = f2pack(sl2, sl2);
+    float m_run = -INFINITY;                     // reference max of scale*log2(e)*s (may lag by <= 2^8)
+    float l_run = 0.f;                           // running denominator relative to m_run
+    Cursor c;
+    c.init(args, nt, n_items);
+    for (int t = 0; c.valid; ++t, c.next(args)) {
+      const int buf = t % kSBuf;
+      const int j = c.j;
+      const int row = c.it.qt * kBM + r;
+      const uint32_t tS = tmem + buf * 128 + lane_off;
+      if (!mbar_wait_warp(&bars->s_full[buf], (t / kSBuf) & 1, st, abort_flag, kSiteSFull)) break;
       tc_fence_after();
-      const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
       uint32_t sr[4][32];
-      __syncwarp();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+      for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
       tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+      for (int q = 0; q < 4; ++q) reg_fence(sr[q]);
 
       const int key0 = j * kBN;
-      const bool need_mask = (key0 + kBN > N) || (args.causal && j == qt);
-      float mx = -INFINITY;
+      if ((key0 + kBN > N) || (args.causal && j == c.it.qt)) {
+        const int lim = min(N, args.causal ? row + 1 : N) - key0;   // keys [key0, key0 + lim) are visible
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+        for (int q = 0; q < 4; ++q)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(sr[c][e]);
-          if (need_mask) {
-            const int key = key0 + c * 32 + e;
-            if (key >= N || (args.causal && key > row)) x = -INFINITY;
-          }
-          sr[c][e] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          for (int e = 0; e < 32; ++e)
+            if (q * 32 + e >= lim) sr[q][e] = __float_as_uint(-INFINITY);
+      }
+      // Row max: four independent three-input max chains.
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          mx0 = fmax3(mx0, __uint_as_float(sr[q][e + 0]), __uint_as_float(sr[q][e + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(sr[q][e + 2]), __uint_as_float(sr[q][e + 3]));
+          mx2 = fmax3(mx2, __uint_as_float(sr[q][e + 4]), __uint_as_float(sr[q][e + 5]));
+          mx3 = fmax3(mx3, __uint_as_float(sr[q][e + 6]), __uint_as_float(sr[q][e + 7]));
         }
       }
-      const float m_new = fmaxf(m_run, mx * sl2);
+      const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      if (j == 0) {
+        m_run = -INFINITY;
+        l_run = 0.f;
+      }
+      const bool need = (j == 0) || (m_cand > m_run + kRescaleThreshold);
+      const float m_new = need ? m_cand : m_run;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2(m_run - m_use);
-      uint32_t pk[64];
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c][e]), sl2, -m_use));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[c][e + 1]), sl2, -m_use));
-          rs += p0 + p1;
-          pk[(c * 32 + e) >> 1] = pack_bf16(p0, p1);
-        }
-      }
-      l_run = l_run * alpha + rs;
+      const float alpha = need ? ex2(m_run - m_use) : 1.f;
       m_run = m_new;
 
-      if (j > 0) {
-        // P V of the previous tile must be done: it frees the P tile and the
-        // O accumulator can be rescaled.
-        if (!mbar_wait_warp(&bars->o_done, (j - 1) & 1, st, abort_flag, kSiteODone)) { ok = false; break; }
+      // P = 2^(s*sl2 - m) in fp32 pairs; row sum in four packed accumulators.
+      const uint64_t negm = f2pack(-m_use, -m_use);
+      uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
+      uint32_t pk[64];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint64_t x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint64_t sv = f2pack(__uint_as_float(sr[q][e + 2 * u]), __uint_as_float(sr[q][e + 2 * u + 1]));
+            float lo, hi;
+            f2unpack(ffma2(sv, sl2x2, negm), lo, hi);
+            lo = ex2(lo);
+            hi = ex2(hi);
+            x[u] = f2pack(lo, hi);
+            pk[(q * 32 + e) / 2 + u] = cvt_bf16x2(lo, hi);
+          }
+          acc0 = fadd2(acc0, x[0]);
+          acc1 = fadd2(acc1, x[1]);
+          acc2 = fadd2(acc2, x[2]);
+          acc3 = fadd2(acc3, x[3]);
+        }
+      }
+      float a0, a1, b0, b1;
+      f2unpack(fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3)), a0, a1);
+      l_run = l_run * alpha + (a0 + a1);
+      (void)b0;
+      (void)b1;
+
+      // P (bf16) over the first 64 columns of this tile's score buffer.
+      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O holds rows relative to the old reference max: rescale it once
+        // P V of the previous tile has landed.
+        if (!mbar_wait_warp(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteORescale)) break;
         tc_fence_after();
-        __syncwarp();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        const uint64_t al2 = f2pack(alpha, alpha);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + lane_off + c * 32, o);
-            tmem_wait_ld();
-            reg_fence(o);
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tO + lane_off + q * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tO + lane_off + c * 32, o);
+          for (int e = 0; e < 32; e += 2) {
+            float lo, hi;
+            f2unpack(fmul2(f2pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), al2), lo, hi);
+            o[e] = __float_as_uint(lo);
+            o[e + 1] = __float_as_uint(hi);
           }
-          tmem_wait_st();
+          tmem_st32(tO + lane_off + q * 32, o);
         }
       }
-      // P row r -> shared memory, two 64-key column blocks, swizzled.
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-#pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16) {
-          const int base = a * 32 + c16 * 4;
-          st_shared_v4(sP + a * kBlockBytes + swz128(r, c16), pk[base], pk[base + 1], pk[base + 2], pk[base + 3]);
-        }
-      }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->p_full);
-    }
-    if (ok && mbar_wait_warp(&bars->o_done, (n_kv - 1) & 1, st, abort_flag, kSiteODone)) {
-      tc_fence_after();
-      const float inv_l = 1.f / l_run;
-      const size_t head = (size_t)b * args.Hq + h;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.o) + (head * N + (size_t)row) * D;
-      __syncwarp();
+      mbar_arrive(&bars->p_full[buf]);
+
+      if (j == c.it.n - 1) {
+        // ------------------------------------------------ epilogue of the item
+        if (!mbar_wait_warp(&bars->o_done[t & 1], (t >> 1) & 1, st, abort_flag, kSiteOLast)) break;
+        tc_fence_after();
+        uint32_t o[D / 32][32];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
+        for (int q = 0; q < D / 32; ++q) tmem_ld32(tO + lane_off + q * 32, o[q]);
         tmem_wait_ld();
-        reg_fence(o);
-        if (row < N) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(o[v * 8 + 0]) * inv_l, __uint_as_float(o[v * 8 + 1]) * inv_l);
-            w.y = pack_bf16(__uint_as_float(o[v * 8 + 2]) * inv_l, __uint_as_float(o[v * 8 + 3]) * inv_l);
-            w.z = pack_bf16(__uint_as_float(o[v * 8 + 4]) * inv_l, __uint_as_float(o[v * 8 + 5]) * inv_l);
-            w.w = pack_bf16(__uint_as_float(o[v * 8 + 6]) * inv_l, __uint_as_float(o[v * 8 + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + c * 32 + v * 8) = w;
+        for (int q = 0; q < D / 32; ++q) reg_fence(o[q]);
+        tc_fence_before();
+        mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
+        const float inv_l = 1.f / l_run;
+        const size_t head = (size_t)c.it.b * args.Hq + c.it.h;
+        if (row < N) {
+          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.o) + (head * N + (size_t)row) * D;
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 0]) * inv_l, __uint_as_float(o[q][v * 8 + 1]) * inv_l);
+              w.y = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 2]) * inv_l, __uint_as_float(o[q][v * 8 + 3]) * inv_l);
+              w.z = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 4]) * inv_l, __uint_as_float(o[q][v * 8 + 5]) * inv_l);
+              w.w = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 6]) * inv_l, __uint_as_float(o[q][v * 8 + 7]) * inv_l);
+              *reinterpret_cast<uint4*>(orow + q * 32 + v * 8) = w;
+            }
           }
+          args.lse[head * N + row] = (m_run + __log2f(l_run)) * 0.69314718055994530942f;
         }
       }
-      if (row < N) args.lse[head * N + row] = (m_run + __log2f(l_run)) * 0.69314718055994530942f;
     }
   }
 
@@ -313,21 +451,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const FwdArgs& a, const DevStatus& st, cudaStream_t stream) {
-  using L = FwdSmem<D>;
+                                const FwdArgs& a, const DevStatus& st, int num_sms, cudaStream_t stream) {
+  using L = FwdCfg<D>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
+  static_assert(sizeof(Bars) <= 512, "barrier block");
   cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  const int nt = (a.N + kBM - 1) / kBM;
-  dim3 grid(a.Hq, a.B, nt);
+  const long long nt = (a.N + kBM - 1) / kBM;
+  const long long items = nt * a.Hq * a.B;
+  const int grid = (int)(items < num_sms ? items : num_sms);
   fa_fwd_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, a, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
-                       const DevStatus& st, cudaStream_t stream) {
-  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, a, st, stream);
-  return launch_fwd_d<128>(tq, tk, tv, a, st, stream);
+                       const DevStatus& st, int num_sms, cudaStream_t stream) {
+  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, a, st, num_sms, stream);
+  return launch_fwd_d<128>(tq, tk, tv, a, st, num_sms, stream);
 }
 
 }  // namespace fa

@@ -31,7 +31,7 @@ struct BwdArgs {
 };
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
-                       const DevStatus& st, cudaStream_t stream);
+                       const DevStatus& st, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dO, float* drow, float* dq_accum, long long rows,
                                   int num_sms, cudaStream_t stream);

@@ -25,8 +25,9 @@
  *       lse          : fp32 [B, Hq,  N]
  *   - Every pointer must be 16-byte aligned (FA_ERR_MISALIGNED otherwise).
  *   - d must be 64 or 128 (FA_ERR_UNSUPPORTED_HEADDIM otherwise);
- *     B, Hq, Hkv, N >= 1, Hq % Hkv == 0, B <= 65535 and N <= 8388480
- *     (65535 tiles of 128 rows) (FA_ERR_BAD_SHAPE otherwise).
+ *     B, Hq, Hkv, N >= 1, Hq % Hkv == 0, B <= 65535, N <= 8388480
+ *     (65535 tiles of 128 rows) and ceil(N/128)*Hq*B < 2^31
+ *     (FA_ERR_BAD_SHAPE otherwise).
  *   - scale must be finite and > 0 (FA_ERR_BAD_ARGUMENT otherwise).
  *   - Outputs must not overlap any input or each other (FA_ERR_ALIASING).
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
