@@ -291,10 +291,11 @@ def run_ours(args, w):
         call(fa.fa_fwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, Hq, Hkv, N, d, w.causal, w.scale, sh), "fwd")
         if ev:
             ev[1].record(stream)
-        call(fa.fa_bwd_preprocess(ptr(o), ptr(do), B, Hq, Hkv, N, d, ptr(ws), ws_bytes, sh), "bwd_preprocess")
+        call(fa.fa_bwd_preprocess(ptr(o), ptr(do), ptr(lse), B, Hq, Hkv, N, d, ptr(ws), ws_bytes, sh),
+             "bwd_preprocess")
         if ev:
             ev[2].record(stream)
-        call(fa.fa_bwd_dkdv(ptr(q), ptr(k), ptr(v), ptr(do), ptr(lse), ptr(dk), ptr(dv), B, Hq, Hkv, N, d,
+        call(fa.fa_bwd_dkdv(ptr(q), ptr(k), ptr(v), ptr(do), ptr(dk), ptr(dv), B, Hq, Hkv, N, d,
                             w.causal, w.scale, ptr(ws), ws_bytes, sh), "bwd_dkdv")
         if ev:
             ev[3].record(stream)

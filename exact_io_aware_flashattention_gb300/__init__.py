@@ -58,8 +58,8 @@ _SIGNATURES = {
     "fa_fwd": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p], _i),
     "fa_bwd_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
     "fa_bwd": ([_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p, _sz, _p], _i),
-    "fa_bwd_preprocess": ([_p, _p, _i, _i, _i, _i, _i, _p, _sz, _p], _i),
-    "fa_bwd_dkdv": ([_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p, _sz, _p], _i),
+    "fa_bwd_preprocess": ([_p, _p, _p, _i, _i, _i, _i, _i, _p, _sz, _p], _i),
+    "fa_bwd_dkdv": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p, _sz, _p], _i),
     "fa_bwd_dq_convert": ([_p, _i, _i, _i, _i, _i, _f, _p, _sz, _p], _i),
     "fa_strerror": ([_i], ctypes.c_char_p),
     "fa_last_device_status": ([_p, ctypes.POINTER(ctypes.c_int)], _i),
@@ -117,12 +117,12 @@ def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, wor
                                  workspace, workspace_bytes, stream)
 
 
-def fa_bwd_preprocess(o, do, B, Hq, Hkv, N, d, workspace, workspace_bytes, stream):
-    return load_library().fa_bwd_preprocess(o, do, B, Hq, Hkv, N, d, workspace, workspace_bytes, stream)
+def fa_bwd_preprocess(o, do, lse, B, Hq, Hkv, N, d, workspace, workspace_bytes, stream):
+    return load_library().fa_bwd_preprocess(o, do, lse, B, Hq, Hkv, N, d, workspace, workspace_bytes, stream)
 
 
-def fa_bwd_dkdv(q, k, v, do, lse, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, stream):
-    return load_library().fa_bwd_dkdv(q, k, v, do, lse, dk, dv, B, Hq, Hkv, N, d, int(causal), float(scale),
+def fa_bwd_dkdv(q, k, v, do, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, stream):
+    return load_library().fa_bwd_dkdv(q, k, v, do, dk, dv, B, Hq, Hkv, N, d, int(causal), float(scale),
                                       workspace, workspace_bytes, stream)
 
 

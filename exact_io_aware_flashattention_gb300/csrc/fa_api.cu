@@ -118,14 +118,18 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t elems(int B, int H, int N, int d) { return (size_t)B * H * N * d; }
 
+// Backward workspace: fp32 dQ accumulator [B,Hq,N,d], then LSE*log2(e) and
+// D = rowsum(dO*O), each fp32 [B*Hq, ntp] with ntp = ceil(N/128)*128.
 struct WsLayout {
-  size_t dq_off, dr_off, total;
+  size_t dq_off, lse2_off, dr_off, total;
 };
 WsLayout ws_layout(int B, int Hq, int N, int d) {
+  const size_t ntp = (size_t)((N + 127) / 128) * 128;
   WsLayout w;
   w.dq_off = 0;
-  w.dr_off = align256(elems(B, Hq, N, d) * 4);
-  w.total = w.dr_off + align256((size_t)B * Hq * N * 4);
+  w.lse2_off = align256(elems(B, Hq, N, d) * 4);
+  w.dr_off = w.lse2_off + align256((size_t)B * Hq * ntp * 4);
+  w.total = w.dr_off + align256((size_t)B * Hq * ntp * 4);
   return w;
 }
 
@@ -148,18 +152,18 @@ fa_status launch_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ER
     if (_s != FA_OK) return _s;     \
   } while (0)
 
-fa_status validate_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse, void* dk,
-                        void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
-                        const void* workspace, size_t workspace_bytes) {
-  if (!q || !k || !v || !dO || !lse || !dk || !dv || !workspace) return FA_ERR_NULL_PTR;
+fa_status validate_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B,
+                        int Hq, int Hkv, int N, int d, int causal, float scale, const void* workspace,
+                        size_t workspace_bytes) {
+  if (!q || !k || !v || !dO || !dk || !dv || !workspace) return FA_ERR_NULL_PTR;
   FA_TRY(check_shape(B, Hq, Hkv, N, d));
   FA_TRY(check_scale(causal, scale));
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) || !aligned16(dk) ||
-      !aligned16(dv) || !aligned16(workspace))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(workspace))
     return FA_ERR_MISALIGNED;
   if (workspace_bytes < ws_layout(B, Hq, N, d).total) return FA_ERR_WORKSPACE_TOO_SMALL;
   const size_t qb = elems(B, Hq, N, d) * 2, kb = elems(B, Hkv, N, d) * 2;
-  const Range ins[] = {range(q, qb), range(k, kb), range(v, kb), range(dO, qb), range(lse, (size_t)B * Hq * N * 4)};
+  const Range ins[] = {range(q, qb), range(k, kb), range(v, kb), range(dO, qb)};
   const Range outs[] = {range(dk, kb), range(dv, kb), range(workspace, ws_layout(B, Hq, N, d).total)};
   for (const Range& o : outs)
     for (const Range& i : ins)
@@ -233,28 +237,29 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
       fa::launch_fwd(d, tq, tk, tv, a, dev_status(ds), ds->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
-fa_status fa_bwd_preprocess(const void* o, const void* dO, int B, int Hq, int Hkv, int N, int d, void* workspace,
-                            size_t workspace_bytes, void* stream) {
-  if (!o || !dO || !workspace) return FA_ERR_NULL_PTR;
+fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, int B, int Hq, int Hkv, int N, int d,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if (!o || !dO || !lse || !workspace) return FA_ERR_NULL_PTR;
   FA_TRY(check_shape(B, Hq, Hkv, N, d));
-  if (!aligned16(o) || !aligned16(dO) || !aligned16(workspace)) return FA_ERR_MISALIGNED;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(lse) || !aligned16(workspace)) return FA_ERR_MISALIGNED;
   const WsLayout w = ws_layout(B, Hq, N, d);
   if (workspace_bytes < w.total) return FA_ERR_WORKSPACE_TOO_SMALL;
   const size_t qb = elems(B, Hq, N, d) * 2;
   const Range rw = range(workspace, w.total);
-  if (overlap(rw, range(o, qb)) || overlap(rw, range(dO, qb))) return FA_ERR_ALIASING;
+  if (overlap(rw, range(o, qb)) || overlap(rw, range(dO, qb)) || overlap(rw, range(lse, (size_t)B * Hq * N * 4)))
+    return FA_ERR_ALIASING;
   DeviceState* ds = nullptr;
   FA_TRY(device_state(&ds));
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  return launch_status(fa::launch_bwd_preprocess(d, o, dO, reinterpret_cast<float*>(ws + w.dr_off),
-                                                 reinterpret_cast<float*>(ws + w.dq_off), (long long)B * Hq * N,
-                                                 ds->num_sms, static_cast<cudaStream_t>(stream)));
+  return launch_status(fa::launch_bwd_preprocess(
+      d, o, dO, lse, reinterpret_cast<float*>(ws + w.lse2_off), reinterpret_cast<float*>(ws + w.dr_off),
+      reinterpret_cast<float*>(ws + w.dq_off), (long long)B * Hq, N, ds->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
-fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse, void* dk,
-                      void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* workspace,
-                      size_t workspace_bytes, void* stream) {
-  FA_TRY(validate_dkdv(q, k, v, dO, lse, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B, int Hq,
+                      int Hkv, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  FA_TRY(validate_dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
   DeviceState* ds = nullptr;
   FA_TRY(device_state(&ds));
   CUtensorMap tq, tk, tv, tdo;
@@ -265,7 +270,7 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
   const WsLayout w = ws_layout(B, Hq, N, d);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   fa::BwdArgs a;
-  a.lse = lse;
+  a.lse2 = reinterpret_cast<const float*>(ws + w.lse2_off);
   a.drow = reinterpret_cast<const float*>(ws + w.dr_off);
   a.dq_accum = reinterpret_cast<float*>(ws + w.dq_off);
   a.dk = dk;
@@ -300,9 +305,9 @@ fa_status fa_bwd_dq_convert(void* dq, int B, int Hq, int Hkv, int N, int d, floa
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                  void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                  void* workspace, size_t workspace_bytes, void* stream) {
-  if (!o || !dq) return FA_ERR_NULL_PTR;
-  FA_TRY(validate_dkdv(q, k, v, dO, lse, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
-  if (!aligned16(o) || !aligned16(dq)) return FA_ERR_MISALIGNED;
+  if (!o || !dq || !lse) return FA_ERR_NULL_PTR;
+  FA_TRY(validate_dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
+  if (!aligned16(o) || !aligned16(dq) || !aligned16(lse)) return FA_ERR_MISALIGNED;
   const size_t qb = elems(B, Hq, N, d) * 2, kb = elems(B, Hkv, N, d) * 2;
   const Range rdq = range(dq, qb);
   const Range others[] = {range(q, qb),  range(k, kb),  range(v, kb),  range(o, qb), range(dO, qb),
@@ -311,11 +316,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   for (const Range& r : others)
     if (overlap(rdq, r)) return FA_ERR_ALIASING;
   const Range ro = range(o, qb);
-  if (overlap(ro, range(dk, kb)) || overlap(ro, range(dv, kb)) ||
-      overlap(ro, range(workspace, ws_layout(B, Hq, N, d).total)))
-    return FA_ERR_ALIASING;
-  FA_TRY(fa_bwd_preprocess(o, dO, B, Hq, Hkv, N, d, workspace, workspace_bytes, stream));
-  FA_TRY(fa_bwd_dkdv(q, k, v, dO, lse, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, stream));
+  const Range rl = range(lse, (size_t)B * Hq * N * 4), rw = range(workspace, ws_layout(B, Hq, N, d).total);
+  if (overlap(ro, range(dk, kb)) || overlap(ro, range(dv, kb)) || overlap(ro, rw)) return FA_ERR_ALIASING;
+  if (overlap(rl, range(dk, kb)) || overlap(rl, range(dv, kb)) || overlap(rl, rw)) return FA_ERR_ALIASING;
+  FA_TRY(fa_bwd_preprocess(o, dO, lse, B, Hq, Hkv, N, d, workspace, workspace_bytes, stream));
+  FA_TRY(fa_bwd_dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, stream));
   return fa_bwd_dq_convert(dq, B, Hq, Hkv, N, d, scale, workspace, workspace_bytes, stream);
 }
 

@@ -4,24 +4,35 @@
 // 在线 softmax", closing paragraphs).
 //
 // Three kernels on the caller's stream:
-//   1. preprocess: D_i = sum_c dO[i,c] * O[i,c] (warp-shuffle reduction) and
-//      zero the fp32 dQ accumulator.
+//   1. preprocess: D_i = sum_c dO[i,c] * O[i,c] (warp-shuffle reduction),
+//      LSE_i * log2(e), both padded per head to a multiple of 128 rows (+inf
+//      and 0 past N), and zero the fp32 dQ accumulator.
 //   2. dkdv: one CTA owns one 128-key tile of one kv head and loops over every
 //      query head of its group and every 128-query tile that can see it.  dK
 //      and dV accumulate in tensor memory and are written once: no atomics.
-//      Per (query tile, key tile) it recomputes S^T = K Q^T, P^T = exp(S^T -
-//      LSE), dP^T = V dO^T, dS^T = P^T * (dP^T - D), and issues
-//      dV += P^T dO, dK += dS^T Q, dQ_partial = dS K; the dQ partial is added
-//      into the fp32 accumulator (the separate dQ reduction).
+//      Per (query tile, key tile) it recomputes S^T = K Q^T, P^T = 2^(S^T *
+//      scale * log2 e - LSE * log2 e), dP^T = V dO^T, dS^T = P^T (dP^T - D),
+//      and issues dV += P^T dO, dK += dS^T Q, dQ_partial = dS K; the dQ
+//      partial is added into the fp32 accumulator (the separate dQ reduction).
 //   3. dq_convert: dQ = bf16(scale * accumulator).
 //
-// dkdv CTA layout (192 threads):
-//   warp 0     TMA producer (K, V once; Q_i, dO_i per item)
-//   warp 1     TMEM allocator and MMA issuer
-//   warps 2-5  compute warpgroup: thread t owns key row t of the tile for
-//              S^T / dP^T / dK / dV, and query row t for the dQ partial.
-// Tensor memory: S^T (then the dQ partial) at column 0, dP^T at 128,
-// dV at 256, dK at 256 + d.
+// dkdv CTA layout (320 threads):
+//   warp 0      TMA producer: K, V once; per item Q_i, dO_i (2 slots each) and
+//               the item's 128 LSE / D values (bulk copies, 2 slots)
+//   warp 1      TMEM allocator and MMA issuer
+//   warps 2-5   compute warpgroup 0, warps 6-9 compute warpgroup 1: thread t
+//               of a group owns key row t (TMEM lane t) for S^T, dP^T, dK, dV
+//               and query row t for the dQ partial; group g handles query
+//               columns [64g, 64g+64) and head-dim columns [g d/2, (g+1) d/2).
+// Tensor memory: S^T at columns 0-127 (P^T, bf16, is written back over the
+// group's own columns: 0-31 and 64-95) and read there by the dV MMA;
+// dP^T at 128-255, reused for the dQ partial; dV at 256, dK at 256 + d.
+// dS^T (bf16) goes to one shared-memory tile read by both the dK MMA
+// (K-major) and the dQ MMA (as dS, MN-major).
+//
+// Tensor pipe order per item t:  S_t, dP_t, dV_t, dK_t, dQ_t, S_{t+1}, ...
+// S_{t+1} waits for dV_t (it overwrites P^T_t); dP_{t+1} waits until the dQ
+// partial of item t has been read out of the same columns.
 #include "fa_internal.h"
 #include "sm103a.cuh"
 
@@ -30,7 +41,7 @@ namespace fa {
 namespace {
 
 constexpr int kT = 128;             // rows per query tile and per key tile
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kBlockBytes = 128u * 128u;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -39,28 +50,34 @@ struct BwdSmem {
   static constexpr uint32_t kTile = 128u * D * 2u;
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kK + kTile;
-  static constexpr uint32_t kQ = kV + kTile;
-  static constexpr uint32_t kDO = kQ + kTile;
-  static constexpr uint32_t kP = kDO + kTile;
-  static constexpr uint32_t kDS = kP + 128u * 128u * 2u;
-  static constexpr uint32_t kLse = kDS + 128u * 128u * 2u;   // 2 x 128 fp32
-  static constexpr uint32_t kDr = kLse + 1024u;               // 2 x 128 fp32
+  static constexpr uint32_t kQ = kV + kTile;          // 2 slots
+  static constexpr uint32_t kDO = kQ + 2 * kTile;     // 2 slots
+  static constexpr uint32_t kDS = kDO + 2 * kTile;
+  static constexpr uint32_t kLse = kDS + 128u * 128u * 2u;   // 2 slots x 128 fp32
+  static constexpr uint32_t kDr = kLse + 1024u;               // 2 slots x 128 fp32
   static constexpr uint32_t kBar = kDr + 1024u;
   static constexpr uint32_t kBytes = kBar + 256u;
-  static constexpr uint32_t kAlloc = kBytes + 1024u;
 };
 
 enum : int {
-  kSiteKV = 11, kSiteQEmpty, kSiteQFull, kSiteDqEmpty, kSiteDoFull, kSitePFull, kSiteDsFull,
-  kSiteSFull, kSiteDpFull, kSiteDqFull, kSiteDkvDone, kSiteWgSync
+  kSiteKV = 11, kSiteQEmpty, kSiteDoEmpty, kSiteLdEmpty, kSiteQFull, kSiteDvDone, kSiteDoFull, kSiteDqEmpty,
+  kSitePFull, kSiteDsFull, kSiteLdFull, kSiteSFull, kSiteDpFull, kSiteDqFull, kSiteDkvDone
 };
 
 struct Bars {
-  uint64_t kv_full, q_full, do_full, qdo_empty;
-  uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, dkv_done, drain, wg_sync;
+  uint64_t kv_full;
+  uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2], ld_full[2], ld_empty[2];
+  uint64_t s_full, dp_full, p_full, dv_done, ds_full, dq_full, dq_empty, dkv_done, drain;
   uint32_t tmem_base;
   int abort;
 };
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -69,10 +86,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const BwdArgs args, const DevStatus st) {
   using L = BwdSmem<D>;
   constexpr int kAtoms = D / 64;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int kHalfD = D / 2;
+  extern __shared__ __align__(1024) uint8_t smem[];
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBar);
   volatile int* abort_flag = &bars->abort;
+
+  // The swizzled operand tiles need a 1024-byte aligned base.  The dynamic
+  // shared memory of a kernel without static shared memory starts there; if
+  // it ever did not, stop cleanly with an error instead of computing garbage.
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(st, kErrDeviceTimeout, 10);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -88,18 +113,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->do_full, 1);
-    mbar_init(&bars->qdo_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+      mbar_init(&bars->do_full[s], 1);
+      mbar_init(&bars->do_empty[s], 1);
+      mbar_init(&bars->ld_full[s], 1);
+      mbar_init(&bars->ld_empty[s], 256);
+    }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->ds_full, 128);
+    mbar_init(&bars->p_full, 256);
+    mbar_init(&bars->dv_done, 1);
+    mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_empty, 128);
+    mbar_init(&bars->dq_empty, 256);
     mbar_init(&bars->dkv_done, 1);
     mbar_init(&bars->drain, 1);
-    mbar_init(&bars->wg_sync, 128);
     bars->abort = 0;
     mbar_fence_init();
     fence_proxy_async_smem();
@@ -122,8 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sV = smem_u32(smem + L::kV);
   const uint32_t sQ = smem_u32(smem + L::kQ);
   const uint32_t sDO = smem_u32(smem + L::kDO);
-  const uint32_t sP = smem_u32(smem + L::kP);
   const uint32_t sDS = smem_u32(smem + L::kDS);
+  const int ntp = nt * kT;                       // padded rows per head of the LSE / D arrays
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -133,23 +163,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(smem + L::kK + a * kBlockBytes, &tmK, &bars->kv_full, a * 64, j * kT, kvh, b);
         tma_load_4d(smem + L::kV + a * kBlockBytes, &tmV, &bars->kv_full, a * 64, j * kT, kvh, b);
       }
-      int issued = 0;
+      int n_ld[2] = {0, 0}, n_q[2] = {0, 0}, n_do[2] = {0, 0};   // copies issued per slot
       for (int t = 0; t < n_items; ++t) {
         const int h = kvh * G + t / nqi;
         const int i = i0 + t % nqi;
-        if (t > 0 && !mbar_wait(&bars->qdo_empty, (t - 1) & 1, st, abort_flag, kSiteQEmpty)) break;
-        mbar_arrive_expect_tx(&bars->q_full, L::kTile);
+        const int slot = t & 1;
+        const uint32_t ph = ((t >> 1) - 1) & 1;   // phase of this slot's previous use
+        if (t >= 2 && !mbar_wait(&bars->ld_empty[slot], ph, st, abort_flag, kSiteLdEmpty)) break;
+        const size_t roff = ((size_t)b * args.Hq + h) * ntp + (size_t)i * kT;
+        mbar_arrive_expect_tx(&bars->ld_full[slot], 1024u);
+        bulk_load(smem + L::kLse + slot * 512, args.lse2 + roff, 512u, &bars->ld_full[slot]);
+        bulk_load(smem + L::kDr + slot * 512, args.drow + roff, 512u, &bars->ld_full[slot]);
+        ++n_ld[slot];
+        if (t >= 2 && !mbar_wait(&bars->q_empty[slot], ph, st, abort_flag, kSiteQEmpty)) break;
+        mbar_arrive_expect_tx(&bars->q_full[slot], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
-          tma_load_4d(smem + L::kQ + a * kBlockBytes, &tmQ, &bars->q_full, a * 64, i * kT, h, b);
-        mbar_arrive_expect_tx(&bars->do_full, L::kTile);
+          tma_load_4d(smem + L::kQ + slot * L::kTile + a * kBlockBytes, &tmQ, &bars->q_full[slot], a * 64, i * kT,
+                      h, b);
+        ++n_q[slot];
+        if (t >= 2 && !mbar_wait(&bars->do_empty[slot], ph, st, abort_flag, kSiteDoEmpty)) break;
+        mbar_arrive_expect_tx(&bars->do_full[slot], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
-          tma_load_4d(smem + L::kDO + a * kBlockBytes, &tmDO, &bars->do_full, a * 64, i * kT, h, b);
-        ++issued;
+          tma_load_4d(smem + L::kDO + slot * L::kTile + a * kBlockBytes, &tmDO, &bars->do_full[slot], a * 64,
+                      i * kT, h, b);
+        ++n_do[slot];
       }
+      // Every copy issued must have landed before the CTA may exit.
       mbar_wait_drain(&bars->kv_full, 0, st.timeout_ns);
-      if (issued) {
-        mbar_wait_drain(&bars->q_full, (issued - 1) & 1, st.timeout_ns);
-        mbar_wait_drain(&bars->do_full, (issued - 1) & 1, st.timeout_ns);
+      for (int s = 0; s < 2; ++s) {
+        if (n_ld[s]) mbar_wait_drain(&bars->ld_full[s], (n_ld[s] - 1) & 1, st.timeout_ns);
+        if (n_q[s]) mbar_wait_drain(&bars->q_full[s], (n_q[s] - 1) & 1, st.timeout_ns);
+        if (n_do[s]) mbar_wait_drain(&bars->do_full[s], (n_do[s] - 1) & 1, st.timeout_ns);
       }
     }
   } else if (warp == 1) {
@@ -160,38 +204,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idMM = idesc_bf16(128, D, true, true);       // dQ
       bool ok = mbar_wait(&bars->kv_full, 0, st, abort_flag, kSiteKV);
       for (int t = 0; ok && t < n_items; ++t) {
-        const uint32_t ph = t & 1;
-        if (!mbar_wait(&bars->q_full, ph, st, abort_flag, kSiteQFull)) break;
-        if (t > 0 && !mbar_wait(&bars->dq_empty, (t - 1) & 1, st, abort_flag, kSiteDqEmpty)) break;
+        const int slot = t & 1;
+        const uint32_t sph = (t >> 1) & 1;   // slot phase
+        const uint32_t ph = t & 1;           // per-item barrier phase
+        const uint32_t pph = (t - 1) & 1;    // previous item's phase
+        const uint32_t qa = sQ + slot * L::kTile, da = sDO + slot * L::kTile;
+        if (!mbar_wait(&bars->q_full[slot], sph, st, abort_flag, kSiteQFull)) break;
+        if (t > 0 && !mbar_wait(&bars->dv_done, pph, st, abort_flag, kSiteDvDone)) break;
         tc_fence_after();
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
-          mma_bf16_ss(tS, desc_kmajor(sK, k16, kBlockBytes), desc_kmajor(sQ, k16, kBlockBytes), idSS, k16 > 0);
+          mma_bf16_ss(tS, desc_kmajor(sK, k16, kBlockBytes), desc_kmajor(qa, k16, kBlockBytes), idSS, k16 > 0);
         mma_commit(&bars->s_full);
-        if (!mbar_wait(&bars->do_full, ph, st, abort_flag, kSiteDoFull)) break;
+        if (!mbar_wait(&bars->do_full[slot], sph, st, abort_flag, kSiteDoFull)) break;
+        if (t > 0 && !mbar_wait(&bars->dq_empty, pph, st, abort_flag, kSiteDqEmpty)) break;
         tc_fence_after();
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
-          mma_bf16_ss(tDP, desc_kmajor(sV, k16, kBlockBytes), desc_kmajor(sDO, k16, kBlockBytes), idSS, k16 > 0);
+          mma_bf16_ss(tDP, desc_kmajor(sV, k16, kBlockBytes), desc_kmajor(da, k16, kBlockBytes), idSS, k16 > 0);
         mma_commit(&bars->dp_full);
         if (!mbar_wait(&bars->p_full, ph, st, abort_flag, kSitePFull)) break;
         tc_fence_after();
+        // P^T for query columns 16*k16.. lives at column (k16/4)*64 + (k16%4)*8.
 #pragma unroll
         for (int k16 = 0; k16 < kT / 16; ++k16)
-          mma_bf16_ss(tDV, desc_kmajor(sP, k16, kBlockBytes), desc_mnmajor(sDO, k16, kBlockBytes), idKM,
+          mma_bf16_ts(tDV, tS + (k16 >> 2) * 64 + (k16 & 3) * 8, desc_mnmajor(da, k16, kBlockBytes), idKM,
                       (t > 0 || k16 > 0) ? 1u : 0u);
+        mma_commit(&bars->dv_done);
+        mma_commit(&bars->do_empty[slot]);
         if (!mbar_wait(&bars->ds_full, ph, st, abort_flag, kSiteDsFull)) break;
         tc_fence_after();
 #pragma unroll
         for (int k16 = 0; k16 < kT / 16; ++k16)
-          mma_bf16_ss(tDK, desc_kmajor(sDS, k16, kBlockBytes), desc_mnmajor(sQ, k16, kBlockBytes), idKM,
+          mma_bf16_ss(tDK, desc_kmajor(sDS, k16, kBlockBytes), desc_mnmajor(qa, k16, kBlockBytes), idKM,
                       (t > 0 || k16 > 0) ? 1u : 0u);
 #pragma unroll
         for (int k16 = 0; k16 < kT / 16; ++k16)
-          mma_bf16_ss(tS, desc_mnmajor(sDS, k16, kBlockBytes), desc_mnmajor(sK, k16, kBlockBytes), idMM,
+          mma_bf16_ss(tDP, desc_mnmajor(sDS, k16, kBlockBytes), desc_mnmajor(sK, k16, kBlockBytes), idMM,
                       k16 > 0 ? 1u : 0u);
         mma_commit(&bars->dq_full);
-        mma_commit(&bars->qdo_empty);
+        mma_commit(&bars->q_empty[slot]);
       }
       mma_commit(&bars->dkv_done);
       mma_commit(&bars->drain);
@@ -199,115 +251,118 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ compute
+    const int g = (warp - 2) >> 2;                 // warpgroup 0 or 1
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const int key = j * kT + r;
+    const int c0 = g * 64;                         // this group's query columns
     const float sl2 = args.scale_log2;
-    float* sLse = reinterpret_cast<float*>(smem + L::kLse);
-    float* sDr = reinterpret_cast<float*>(smem + L::kDr);
-    const float* lse_g = reinterpret_cast<const float*>(args.lse);
+    const uint64_t sl2x2 = f2pack(sl2, sl2);
     bool ok = true;
     for (int t = 0; t < n_items; ++t) {
+      const int slot = t & 1;
       const uint32_t ph = t & 1;
       const int h = kvh * G + t / nqi;
       const int i = i0 + t % nqi;
-      const size_t head = (size_t)b * args.Hq + h;
-      const int qrow = i * kT + r;
-      float* lse_t = sLse + (t & 1) * 128;
-      float* dr_t = sDr + (t & 1) * 128;
-      lse_t[r] = (qrow < N) ? lse_g[head * N + qrow] * kLog2e : INFINITY;
-      dr_t[r] = (qrow < N) ? args.drow[head * N + qrow] : 0.f;
-      // All 128 threads have staged this item's LSE / D (and are done with
-      // the buffer's previous use two items ago).
-      mbar_arrive(&bars->wg_sync);
-      if (!mbar_wait_warp(&bars->wg_sync, ph, st, abort_flag, kSiteWgSync)) { ok = false; break; }
-
+      const float* lse_t = reinterpret_cast<const float*>(smem + L::kLse + slot * 512) + c0;
+      const float* dr_t = reinterpret_cast<const float*>(smem + L::kDr + slot * 512) + c0;
+      if (!mbar_wait_warp(&bars->ld_full[slot], (t >> 1) & 1, st, abort_flag, kSiteLdFull)) { ok = false; break; }
       if (!mbar_wait_warp(&bars->s_full, ph, st, abort_flag, kSiteSFull)) { ok = false; break; }
       tc_fence_after();
-      uint32_t pr[4][32];
-      __syncwarp();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, pr[c]);
+      uint32_t pr[2][32];
+      tmem_ld32(tS + lane_off + c0, pr[0]);
+      tmem_ld32(tS + lane_off + c0 + 32, pr[1]);
       tmem_wait_ld();
+      reg_fence(pr[0]);
+      reg_fence(pr[1]);
+      // P^T[key, q] = 2^(s * sl2 - lse2[q]); zero where the key is past N or
+      // (diagonal tile, causal) after the query.  Query rows past N have
+      // lse2 = +inf in the padded array, which gives 0.
+      int lim = 64;                                // visible query columns are [c0 + 64 - lim, c0 + 64)
+      if (key >= N) lim = 0;
+      else if (args.causal && i == j) lim = min(64, max(0, c0 + 64 - r));
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence(pr[c]);
-      const bool key_valid = key < N;
-      const bool diag = args.causal && (i == j);
+      for (int q = 0; q < 2; ++q) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = c * 32 + e;
-          float p = ex2(fmaf(__uint_as_float(pr[c][e]), sl2, -lse_t[col]));
-          if (!key_valid || (diag && key > i * kT + col)) p = 0.f;
-          pr[c][e] = __float_as_uint(p);
+        for (int e = 0; e < 32; e += 2) {
+          const int col = q * 32 + e;
+          const float4 l4 = *reinterpret_cast<const float4*>(lse_t + (col & ~3));
+          const float la = (col & 2) ? l4.z : l4.x;
+          const float lb = (col & 2) ? l4.w : l4.y;
+          float lo, hi;
+          f2unpack(ffma2(f2pack(__uint_as_float(pr[q][e]), __uint_as_float(pr[q][e + 1])), sl2x2,
+                         f2pack(-la, -lb)),
+                   lo, hi);
+          lo = (col >= 64 - lim) ? ex2(lo) : 0.f;
+          hi = (col + 1 >= 64 - lim) ? ex2(hi) : 0.f;
+          pr[q][e] = __float_as_uint(lo);
+          pr[q][e + 1] = __float_as_uint(hi);
+          pk[col >> 1] = cvt_bf16x2(lo, hi);
         }
       }
-      // P^T row -> shared memory (bf16, swizzled)
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-#pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16) {
-          const int col = a * 64 + c16 * 8;
-          const uint32_t* x = &pr[col >> 5][col & 31];
-          st_shared_v4(sP + a * kBlockBytes + swz128(r, c16),
-                       pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                       pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                       pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                       pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
-        }
-      }
-      fence_proxy_async_smem();
+      tmem_st32(tS + lane_off + c0, pk);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full);
 
       if (!mbar_wait_warp(&bars->dp_full, ph, st, abort_flag, kSiteDpFull)) { ok = false; break; }
       tc_fence_after();
-      __syncwarp();
+      uint32_t dp[2][32];
+      tmem_ld32(tDP + lane_off + c0, dp[0]);
+      tmem_ld32(tDP + lane_off + c0 + 32, dp[1]);
+      tmem_wait_ld();
+      reg_fence(dp[0]);
+      reg_fence(dp[1]);
+      uint32_t ds[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t dp[32];
-        tmem_ld32(tDP + lane_off + c * 32, dp);
-        tmem_wait_ld();
-        reg_fence(dp);
-        uint32_t ds[16];
+      for (int q = 0; q < 2; ++q) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int col = c * 32 + e;
-          const float d0 = __uint_as_float(pr[c][e]) * (__uint_as_float(dp[e]) - dr_t[col]);
-          const float d1 = __uint_as_float(pr[c][e + 1]) * (__uint_as_float(dp[e + 1]) - dr_t[col + 1]);
-          ds[e >> 1] = pack_bf16(d0, d1);
-        }
-        // 32 columns = 4 chunks of 16 bytes in column block c/2.
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int c16 = (c & 1) * 4 + q4;
-          st_shared_v4(sDS + (c >> 1) * kBlockBytes + swz128(r, c16), ds[q4 * 4], ds[q4 * 4 + 1],
-                       ds[q4 * 4 + 2], ds[q4 * 4 + 3]);
+        for (int e = 0; e < 32; e += 4) {
+          const int col = q * 32 + e;
+          const float4 d4 = *reinterpret_cast<const float4*>(dr_t + col);
+          float a0, a1, a2, a3;
+          f2unpack(fmul2(f2pack(__uint_as_float(pr[q][e]), __uint_as_float(pr[q][e + 1])),
+                         fadd2(f2pack(__uint_as_float(dp[q][e]), __uint_as_float(dp[q][e + 1])),
+                               f2pack(-d4.x, -d4.y))),
+                   a0, a1);
+          f2unpack(fmul2(f2pack(__uint_as_float(pr[q][e + 2]), __uint_as_float(pr[q][e + 3])),
+                         fadd2(f2pack(__uint_as_float(dp[q][e + 2]), __uint_as_float(dp[q][e + 3])),
+                               f2pack(-d4.z, -d4.w))),
+                   a2, a3);
+          ds[col >> 1] = cvt_bf16x2(a0, a1);
+          ds[(col >> 1) + 1] = cvt_bf16x2(a2, a3);
         }
       }
+      // dS^T row -> this group's 64-column block of the shared tile.
+#pragma unroll
+      for (int c16 = 0; c16 < 8; ++c16)
+        st_shared_v4(sDS + g * kBlockBytes + swz128(r, c16), ds[c16 * 4], ds[c16 * 4 + 1], ds[c16 * 4 + 2],
+                     ds[c16 * 4 + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->ds_full);
+      mbar_arrive(&bars->ld_empty[slot]);
 
       if (!mbar_wait_warp(&bars->dq_full, ph, st, abort_flag, kSiteDqFull)) { ok = false; break; }
       tc_fence_after();
-      __syncwarp();
-      float* dq_row = args.dq_accum + (head * N + (size_t)qrow) * D;
+      // dQ partial row r (a query) x this group's head-dim columns.
+      const int qrow = i * kT + r;
+      const size_t head = (size_t)b * args.Hq + h;
+      float* dq_row = args.dq_accum + (head * N + (size_t)qrow) * D + g * kHalfD;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int q = 0; q < kHalfD / 32; ++q) {
         uint32_t v[32];
-        tmem_ld32(tS + lane_off + c * 32, v);
+        tmem_ld32(tDP + lane_off + g * kHalfD + q * 32, v);
         tmem_wait_ld();
         reg_fence(v);
         if (qrow < N) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            atomicAdd(reinterpret_cast<float4*>(dq_row + c * 32 + e),
+          for (int e = 0; e < 32; e += 4)
+            atomicAdd(reinterpret_cast<float4*>(dq_row + q * 32 + e),
                       make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
                                   __uint_as_float(v[e + 3])));
-          }
         }
       }
       tc_fence_before();
@@ -317,29 +372,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && mbar_wait_warp(&bars->dkv_done, 0, st, abort_flag, kSiteDkvDone)) {
       tc_fence_after();
       const size_t kvrow = ((size_t)b * args.Hkv + kvh) * N + (size_t)key;
-      __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(args.dv) + kvrow * D;
-      __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(args.dk) + kvrow * D;
-      __syncwarp();
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {
-        const uint32_t src = (pass == 0 ? tDV : tDK) + lane_off;
-        __nv_bfloat16* dst = pass == 0 ? dv_row : dk_row;
+        const uint32_t src = (pass == 0 ? tDV : tDK) + lane_off + g * kHalfD;
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(pass == 0 ? args.dv : args.dk) + kvrow * D + g * kHalfD;
         const float mul = pass == 0 ? 1.f : args.scale;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int q = 0; q < kHalfD / 32; ++q) {
           uint32_t v[32];
-          tmem_ld32(src + c * 32, v);
+          tmem_ld32(src + q * 32, v);
           tmem_wait_ld();
           reg_fence(v);
           if (key < N) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int c = 0; c < 4; ++c) {
               uint4 w;
-              w.x = pack_bf16(__uint_as_float(v[q * 8 + 0]) * mul, __uint_as_float(v[q * 8 + 1]) * mul);
-              w.y = pack_bf16(__uint_as_float(v[q * 8 + 2]) * mul, __uint_as_float(v[q * 8 + 3]) * mul);
-              w.z = pack_bf16(__uint_as_float(v[q * 8 + 4]) * mul, __uint_as_float(v[q * 8 + 5]) * mul);
-              w.w = pack_bf16(__uint_as_float(v[q * 8 + 6]) * mul, __uint_as_float(v[q * 8 + 7]) * mul);
-              *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = w;
+              w.x = cvt_bf16x2(__uint_as_float(v[c * 8 + 0]) * mul, __uint_as_float(v[c * 8 + 1]) * mul);
+              w.y = cvt_bf16x2(__uint_as_float(v[c * 8 + 2]) * mul, __uint_as_float(v[c * 8 + 3]) * mul);
+              w.z = cvt_bf16x2(__uint_as_float(v[c * 8 + 4]) * mul, __uint_as_float(v[c * 8 + 5]) * mul);
+              w.w = cvt_bf16x2(__uint_as_float(v[c * 8 + 6]) * mul, __uint_as_float(v[c * 8 + 7]) * mul);
+              *reinterpret_cast<uint4*>(dst + q * 32 + c * 8) = w;
             }
           }
         }
@@ -357,21 +409,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // D_i = rowsum(dO_i * O_i) with a shuffle reduction over the D/8 lanes that
-// share a row; also zeroes the dQ accumulator.
+// share a row, LSE_i * log2(e), both written padded to ntp rows per head
+// (rows past N get D = 0 and +inf), and the dQ accumulator zeroed.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __restrict__ o,
                                                                 const uint4* __restrict__ dO,
-                                                                float* __restrict__ drow, float4* __restrict__ dq_accum,
-                                                                long long rows) {
+                                                                const float* __restrict__ lse,
+                                                                float* __restrict__ lse2, float* __restrict__ drow,
+                                                                float4* __restrict__ dq_accum, long long heads, int N,
+                                                                int ntp) {
   constexpr int kTpr = D / 8;  // threads per row, 16 bytes each
-  const long long total = rows * kTpr;
+  const long long total = heads * ntp * kTpr;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i0 = (long long)blockIdx.x * blockDim.x; i0 < total; i0 += stride) {
     const long long idx = i0 + threadIdx.x;
+    const long long prow = idx / kTpr;             // padded row
+    const long long head = prow / ntp;
+    const int n = (int)(prow - head * ntp);
+    const bool valid = idx < total && n < N;
+    const long long row = head * N + n;
     float s = 0.f;
-    if (idx < total) {
-      const uint4 a = o[idx];
-      const uint4 g = dO[idx];
+    if (valid) {
+      const uint4 a = o[row * kTpr + idx % kTpr];
+      const uint4 g = dO[row * kTpr + idx % kTpr];
       const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
       const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
 #pragma unroll
@@ -384,9 +444,12 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __r
     }
 #pragma unroll
     for (int off = kTpr / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (idx < total && (idx % kTpr) == 0) drow[idx / kTpr] = s;
+    if (idx < total && (idx % kTpr) == 0) {
+      drow[prow] = valid ? s : 0.f;
+      lse2[prow] = valid ? lse[row] * kLog2e : INFINITY;
+    }
   }
-  const long long n4 = rows * (D / 4);
+  const long long n4 = heads * N * (D / 4);
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride)
     dq_accum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
@@ -398,10 +461,10 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float4* __
     const float4 a = acc[2 * i];
     const float4 c = acc[2 * i + 1];
     uint4 w;
-    w.x = pack_bf16(a.x * scale, a.y * scale);
-    w.y = pack_bf16(a.z * scale, a.w * scale);
-    w.z = pack_bf16(c.x * scale, c.y * scale);
-    w.w = pack_bf16(c.z * scale, c.w * scale);
+    w.x = cvt_bf16x2(a.x * scale, a.y * scale);
+    w.y = cvt_bf16x2(a.z * scale, a.w * scale);
+    w.z = cvt_bf16x2(c.x * scale, c.y * scale);
+    w.w = cvt_bf16x2(c.z * scale, c.w * scale);
     dq[i] = w;
   }
 }
@@ -412,13 +475,14 @@ template <int D>
 static cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const BwdArgs& a, const DevStatus& st, cudaStream_t stream) {
   using L = BwdSmem<D>;
-  static_assert(L::kAlloc <= 232448, "shared memory budget");
+  static_assert(L::kBytes <= 232448, "shared memory budget");
+  static_assert(sizeof(Bars) <= 256, "barrier block");
   cudaError_t e =
-      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const int nt = (a.N + kT - 1) / kT;
   dim3 grid(a.Hkv, a.B, nt);
-  fa_bwd_dkdv_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, a, st);
+  fa_bwd_dkdv_kernel<D><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, a, st);
   return cudaGetLastError();
 }
 
@@ -436,17 +500,18 @@ static int grid_for(long long work_items, int num_sms) {
   return (int)blocks;
 }
 
-cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dO, float* drow, float* dq_accum, long long rows,
-                                  int num_sms, cudaStream_t stream) {
-  const int grid = grid_for(rows * (d / 8), num_sms);
+cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dO, const float* lse, float* lse2, float* drow,
+                                  float* dq_accum, long long heads, int N, int num_sms, cudaStream_t stream) {
+  const int ntp = (N + kT - 1) / kT * kT;
+  const int grid = grid_for(heads * ntp * (d / 8), num_sms);
   if (d == 64)
     fa_bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(o),
-                                                           static_cast<const uint4*>(dO), drow,
-                                                           reinterpret_cast<float4*>(dq_accum), rows);
+                                                           static_cast<const uint4*>(dO), lse, lse2, drow,
+                                                           reinterpret_cast<float4*>(dq_accum), heads, N, ntp);
   else
     fa_bwd_preprocess_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(o),
-                                                            static_cast<const uint4*>(dO), drow,
-                                                            reinterpret_cast<float4*>(dq_accum), rows);
+                                                            static_cast<const uint4*>(dO), lse, lse2, drow,
+                                                            reinterpret_cast<float4*>(dq_accum), heads, N, ntp);
   return cudaGetLastError();
 }
 

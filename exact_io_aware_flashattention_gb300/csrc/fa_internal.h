@@ -19,8 +19,8 @@ struct FwdArgs {
 };
 
 struct BwdArgs {
-  const void* lse;    // [B, Hq, N] fp32 (natural log, from the forward)
-  const float* drow;  // [B, Hq, N] fp32, rowsum(dO * O) (workspace)
+  const float* lse2;  // [B*Hq, ntp] fp32, LSE * log2(e), padded per head to ntp = ceil(N/128)*128 (workspace)
+  const float* drow;  // [B*Hq, ntp] fp32, rowsum(dO * O), same padding (workspace)
   float* dq_accum;    // [B, Hq, N, d] fp32 (workspace)
   void* dk;           // [B, Hkv, N, d] bf16
   void* dv;           // [B, Hkv, N, d] bf16
@@ -33,8 +33,8 @@ struct BwdArgs {
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
                        const DevStatus& st, int num_sms, cudaStream_t stream);
 
-cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dO, float* drow, float* dq_accum, long long rows,
-                                  int num_sms, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dO, const float* lse, float* lse2, float* drow,
+                                  float* dq_accum, long long heads, int N, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, const DevStatus& st, cudaStream_t stream);

@@ -75,9 +75,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 /*
  * Bytes of device workspace fa_bwd needs: the fp32 dQ accumulator
- * [B,Hq,N,d] followed by the fp32 row term D = rowsum(dO * O) [B,Hq,N], each
- * rounded up to 256 bytes.  Returns 0 for invalid shapes.  O(N * d) per head:
- * no N x N buffer.
+ * [B,Hq,N,d], then LSE*log2(e) and the row term D = rowsum(dO * O), each
+ * fp32 [B*Hq, ceil(N/128)*128]; every part rounded up to 256 bytes.
+ * Returns 0 for invalid shapes.  O(N * d) per head: no N x N buffer.
  */
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
 
@@ -95,14 +95,20 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                  void* workspace, size_t workspace_bytes, void* stream);
 
-/* Backward step 1: D = rowsum(dO * O) into the workspace; zero the dQ accumulator. */
-fa_status fa_bwd_preprocess(const void* o, const void* dO, int B, int Hq, int Hkv, int N, int d, void* workspace,
-                            size_t workspace_bytes, void* stream);
+/*
+ * Backward step 1: D = rowsum(dO * O) and LSE * log2(e) into the workspace
+ * (padded per head to a multiple of 128 rows); zero the dQ accumulator.
+ */
+fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, int B, int Hq, int Hkv, int N, int d,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
-/* Backward step 2: dk, dv (written) and the dQ accumulator (added into). Needs step 1. */
-fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse, void* dk,
-                      void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale, void* workspace,
-                      size_t workspace_bytes, void* stream);
+/*
+ * Backward step 2: dk, dv (written) and the dQ accumulator (added into),
+ * recomputing P from the LSE step 1 staged in the workspace.  Needs step 1.
+ */
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B, int Hq,
+                      int Hkv, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                      void* stream);
 
 /* Backward step 3: dq = bf16(scale * dQ accumulator). Needs step 2. */
 fa_status fa_bwd_dq_convert(void* dq, int B, int Hq, int Hkv, int N, int d, float scale, const void* workspace,

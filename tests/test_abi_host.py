@@ -39,10 +39,12 @@ def test_version_and_strerror(lib):
 
 
 def test_workspace_formula_is_linear_in_n(lib):
-    # dQ accumulator fp32 [B,Hq,N,d] + D fp32 [B,Hq,N], each rounded up to 256 B.
+    # dQ accumulator fp32 [B,Hq,N,d] + LSE*log2e and D, fp32 [B*Hq, ceil(N/128)*128]
+    # each; every part rounded up to 256 B.
     def expect(B, Hq, N, d):
-        a = (B * Hq * N * d * 4 + 255) // 256 * 256
-        return a + (B * Hq * N * 4 + 255) // 256 * 256
+        r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+        ntp = (N + 127) // 128 * 128
+        return r256(B * Hq * N * d * 4) + 2 * r256(B * Hq * ntp * 4)
     for shape in [(1, 1, 1, 128, 64), (4, 16, 16, 2048, 128), (1, 16, 16, 32768, 128), (2, 32, 8, 8192, 128)]:
         B, Hq, Hkv, N, d = shape
         assert fa.fa_bwd_workspace_bytes(B, Hq, Hkv, N, d) == expect(B, Hq, N, d)
@@ -104,7 +106,11 @@ def test_bwd_rejects_bad_arguments(lib):
     assert call(d=32) == fa.FA_ERR_UNSUPPORTED_HEADDIM
     assert call(dv=9 * A + 4) == fa.FA_ERR_MISALIGNED
     assert fa.fa_bwd_dq_convert(None, 1, 2, 1, 64, 128, 0.1, 10 * A, ws, None) == fa.FA_ERR_NULL_PTR
-    assert fa.fa_bwd_preprocess(4 * A, 5 * A, 1, 2, 1, 64, 128, 10 * A, 16, None) == fa.FA_ERR_WORKSPACE_TOO_SMALL
+    assert fa.fa_bwd_preprocess(4 * A, 5 * A, 6 * A, 1, 2, 1, 64, 128, 10 * A, 16, None) == \
+        fa.FA_ERR_WORKSPACE_TOO_SMALL
+    assert fa.fa_bwd_preprocess(4 * A, 5 * A, None, 1, 2, 1, 64, 128, 10 * A, ws, None) == fa.FA_ERR_NULL_PTR
+    assert call(lse=None) == fa.FA_ERR_NULL_PTR
+    assert call(lse=6 * A + 8) == fa.FA_ERR_MISALIGNED
 
 
 def test_selftest_rejects_bad_limit(lib):
