@@ -65,6 +65,7 @@ _SIGNATURES = {
     "fa_last_device_status": ([_p, ctypes.POINTER(ctypes.c_int)], _i),
     "fa_selftest_wait_timeout": ([ctypes.c_ulonglong, _p], _i),
     "fa_version": ([], _i),
+    "fa_last_cuda_error": ([], ctypes.c_char_p),
     "fa_bwd_noalloc": ([_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p], _i),
 }
 
@@ -149,6 +150,10 @@ def fa_version():
     return load_library().fa_version()
 
 
+def fa_last_cuda_error():
+    return load_library().fa_last_cuda_error().decode()
+
+
 def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, stream):
     """fa_bwd without a workspace argument: the scratch is a fixed buffer inside
     the library (for callers that cannot allocate device memory)."""
@@ -182,6 +187,8 @@ def _check(t, name, shape, dtype):
 
 def _raise(status, what):
     if status != FA_OK:
+        if status in (FA_ERR_LAUNCH, FA_ERR_CUDA):
+            what = f"{what} [{fa_last_cuda_error()}]"
         raise FAError(status, what)
 
 

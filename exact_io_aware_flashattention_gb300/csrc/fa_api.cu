@@ -14,6 +14,35 @@
 
 namespace {
 
+// Most recent CUDA runtime error behind an FA_ERR_LAUNCH / FA_ERR_CUDA return
+// on this thread (see fa_last_cuda_error).
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+fa_status launch_status(cudaError_t e) {
+  if (e == cudaSuccess) return FA_OK;
+  t_last_cuda_error = e;
+  return FA_ERR_LAUNCH;
+}
+
+// Records a failing runtime call and returns FA_ERR_CUDA.
+fa_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return FA_OK;
+  t_last_cuda_error = e;
+  return FA_ERR_CUDA;
+}
+
+#define FA_TRY(x)                   \
+  do {                              \
+    fa_status _s = (x);             \
+    if (_s != FA_OK) return _s;     \
+  } while (0)
+
+#define FA_TRY_CUDA(x)                                \
+  do {                                                \
+    const cudaError_t _e = (x);                       \
+    if (_e != cudaSuccess) return cuda_status(_e);    \
+  } while (0)
+
 // First device-side error: code, block, wait site, thread.  Read and cleared
 // by fa_last_device_status.
 __device__ int g_status_words[4];
@@ -56,19 +85,18 @@ unsigned long long default_timeout_ns() {
 
 fa_status device_state(DeviceState** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  FA_TRY_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& s = g_dev[dev];
   if (!s.ready) {
     int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return FA_ERR_CUDA;
+    FA_TRY_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    FA_TRY_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    FA_TRY_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED_DEVICE;
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_words) != cudaSuccess) return FA_ERR_CUDA;
+    FA_TRY_CUDA(cudaGetSymbolAddress(&p, g_status_words));
     if (!g_encode) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -144,13 +172,7 @@ fa_status tmap_bf16(CUtensorMap* m, const void* base, int B, int H, int N, int d
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_LAUNCH;
 }
 
-fa_status launch_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH; }
 
-#define FA_TRY(x)                   \
-  do {                              \
-    fa_status _s = (x);             \
-    if (_s != FA_OK) return _s;     \
-  } while (0)
 
 fa_status validate_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B,
                         int Hq, int Hkv, int N, int d, int causal, float scale, const void* workspace,
@@ -177,6 +199,8 @@ fa_status validate_dkdv(const void* q, const void* k, const void* v, const void*
 extern "C" {
 
 int fa_version(void) { return 100; }
+
+const char* fa_last_cuda_error(void) { return cudaGetErrorString(t_last_cuda_error); }
 
 const char* fa_strerror(fa_status s) {
   switch (s) {
@@ -325,7 +349,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 }
 
 fa_status fa_last_device_status(void* stream, int* detail) {
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  {
+    const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   DeviceState* ds = nullptr;
   FA_TRY(device_state(&ds));
   int words[4] = {0, 0, 0, 0};

@@ -13,19 +13,33 @@
 // units), which keeps every exponent <= 2^8 and skips most rescales.
 //
 // Persistent kernel: one CTA per SM walks work items (query tile, head,
-// batch), heaviest causal tiles first.  CTA layout (224 threads):
-//   warp 0     TMA producer for Q (2 slots) and K (ring of kStagesK)
-//   warp 1     TMEM allocator and tcgen05.mma issuer (one elected thread)
-//   warps 2-5  softmax warpgroup: thread t owns query row t of the tile (TMEM
-//              lane t), so row max and row sum are in-thread reductions
-//   warp 6     TMA producer for V (ring of kStagesV)
-// Tensor memory (512 columns): three fp32 128x128 score buffers at columns
-// 0, 128, 256; the O accumulator (fp32 128 x d) at 384.  P (bf16) is written
-// over the first 64 columns of its own score buffer and read from there by
-// the P V MMA, so P never touches shared memory.  With three buffers the
-// tensor pipe computes S two tiles ahead of P V:
-//   S0 S1 | PV0 S2 | PV1 S3 | PV2 S4 ...
-// and the softmax of tile t has the two MMAs before PV_t to finish.
+// batch), heaviest causal tiles first.  CTA layout (384 threads):
+//   warp 0      TMA producer for Q (2 slots) and K (ring of kStagesK)
+//   warp 1      TMEM allocator; one thread issues the S = Q K^T MMAs
+//   warp 11     one thread issues the O += P V MMAs.  The two issuers touch
+//               disjoint tensor memory and each commit tracks only its own
+//               MMAs, so each waits only for what its MMAs need.
+//   warps 2-5   softmax group 0, warps 6-9 softmax group 1: the groups take
+//               alternate score tiles of the CTA's tile sequence (tile t goes
+//               to group t % 2); thread r of the owning group handles query
+//               row r (TMEM lane r), so row max and row sum are in-thread
+//               reductions.  The running reference max is the only state one
+//               tile needs from the previous one: the owner of tile t hands it
+//               to the owner of tile t+1 through shared memory as soon as it
+//               has its row max, then both groups' exponentials overlap.  Each
+//               group keeps its own part of the row sum; the two parts are
+//               combined in the item's epilogue.
+//   warp 10     TMA producer for V (ring of kStagesV)
+// Tensor memory (512 columns): two fp32 128x128 score buffers at columns 0
+// and 128, two bf16 probability buffers (128 x 128 bf16 = 64 columns) at 256
+// and 320, and the O accumulator (fp32 128 x d) at 384.  Tile t uses score
+// and probability buffer t % 2, so each softmax group always works on "its"
+// buffers.  P V reads P straight from tensor memory (P never touches shared
+// memory).  Tensor pipe order:
+//   S0 S1 | S2 PV0 | S3 PV1 | S4 PV2 ...
+// S_{t+2} is issued as soon as the owner of tile t has loaded S_t into
+// registers; P_t is written once P V_{t-2} has consumed the buffer; neither
+// waits for the tensor pipe to drain.
 #include "fa_internal.h"
 #include "sm103a.cuh"
 
@@ -35,8 +49,8 @@ namespace {
 
 constexpr int kBM = 128;        // query rows per tile
 constexpr int kBN = 128;        // keys per tile
-constexpr int kSBuf = 3;        // score / probability buffers in tensor memory
-constexpr int kThreads = 224;
+constexpr int kSBuf = 2;        // score buffers (and probability buffers) in tensor memory
+constexpr int kThreads = 384;
 constexpr uint32_t kBlockBytes = 128u * 128u;   // one 64-column block of a 128-row bf16 tile
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -48,25 +62,28 @@ struct FwdCfg {
   static constexpr uint32_t kQ = 0;                              // 2 slots
   static constexpr uint32_t kK = kQ + 2u * kTile;
   static constexpr uint32_t kV = kK + kStagesK * kTile;
-  static constexpr uint32_t kBar = kV + kStagesV * kTile;
+  static constexpr uint32_t kMref = kV + kStagesV * kTile;     // reference-max hand-off, 2 x 128 fp32
+  static constexpr uint32_t kLx = kMref + 1024u;               // row-sum hand-off, 2 x 128 fp32
+  static constexpr uint32_t kBar = kLx + 1024u;
   static constexpr uint32_t kBytes = kBar + 512u;
-  static constexpr uint32_t kAlloc = kBytes + 1024u;            // slack for 1024-byte alignment
 };
 
 // Wait-site ids reported in the status words.
 enum : int {
   kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSitePFull, kSiteVFull, kSiteOFree,
-  kSiteOPrev, kSiteSFull, kSiteORescale, kSiteOLast
+  kSiteSFree, kSiteSFull, kSiteORescale, kSiteOLast, kSiteHand, kSiteLx, kSitePPrev
 };
 
 struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[4], k_empty[4];
   uint64_t v_full[4], v_empty[4];
-  uint64_t s_full[kSBuf], p_full[kSBuf];
+  uint64_t s_full[kSBuf], s_free[kSBuf], p_full[kSBuf];
   uint64_t o_done[2];
   uint64_t o_free;
-  uint64_t drain;
+  uint64_t hand[2];         // reference max of tile t published (by tile parity)
+  uint64_t lx[2];           // row-sum part of the non-owner group published (by multi-tile item parity)
+  uint64_t drain_s, drain_pv;
   uint32_t tmem_base;
   int abort;
 };
@@ -122,10 +139,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = FwdCfg<D>;
   constexpr int kAtoms = D / 64;
   constexpr int SK = L::kStagesK, SV = L::kStagesV;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBar);
   volatile int* abort_flag = &bars->abort;
+  // The swizzled operand tiles need a 1024-byte aligned base.  The dynamic
+  // shared memory of a kernel without static shared memory starts there; if
+  // it ever did not, stop cleanly with an error instead of computing garbage.
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(st, kErrDeviceTimeout, 0);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -138,6 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
       mbar_init(&bars->o_done[i], 1);
+      mbar_init(&bars->hand[i], 128);
+      mbar_init(&bars->lx[i], 128);
     }
     for (int s = 0; s < SK; ++s) {
       mbar_init(&bars->k_full[s], 1);
@@ -149,10 +174,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kSBuf; ++s) {
       mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_free[s], 128);
       mbar_init(&bars->p_full[s], 128);
     }
     mbar_init(&bars->o_free, 128);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain_s, 1);
+    mbar_init(&bars->drain_pv, 1);
     bars->abort = 0;
     mbar_fence_init();
     fence_proxy_async_smem();
@@ -206,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(&bars->k_full[s], (last / SK) & 1, st.timeout_ns);
       }
     }
-  } else if (warp == 6) {
+  } else if (warp == 10) {
     // ------------------------------------------------------ V producer
     if (lane == 0) {
       int vt = 0;
@@ -228,23 +255,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------ S issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
-      constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
       Cursor sc;
       sc.init(args, nt, n_items);
-      int ts = 0;   // global index of the next score tile to issue
-      // S_ts = Q K^T into buffer ts % 3.  The caller guarantees the buffer's
-      // previous P has been consumed.
-      auto issue_s = [&]() -> bool {
-        if (!sc.valid) return true;
+      for (int ts = 0; sc.valid; ++ts, sc.next(args)) {
         const int buf = ts % kSBuf;
+        // S_ts reuses score buffer ts % 2 once the owner of tile ts-2 has read it.
+        if (ts >= 2 && !mbar_wait(&bars->s_free[buf], ((ts - 2) / kSBuf) & 1, st, abort_flag, kSiteSFree)) break;
         if (sc.j == 0 &&
             !mbar_wait(&bars->q_full[sc.li & 1], (sc.li >> 1) & 1, st, abort_flag, kSiteQFull))
-          return false;
+          break;
         const int s = ts % SK;
-        if (!mbar_wait(&bars->k_full[s], (ts / SK) & 1, st, abort_flag, kSiteKFull)) return false;
+        if (!mbar_wait(&bars->k_full[s], (ts / SK) & 1, st, abort_flag, kSiteKFull)) break;
         tc_fence_after();
         const uint32_t qa = sQ + (sc.li & 1) * L::kTile;
         const uint32_t ka = sK + s * L::kTile;
@@ -255,14 +279,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars->s_full[buf]);
         mma_commit(&bars->k_empty[s]);
         if (sc.j == sc.it.n - 1) mma_commit(&bars->q_empty[sc.li & 1]);
-        ++ts;
-        sc.next(args);
-        return true;
-      };
-      bool ok = issue_s() && issue_s();
+      }
+      // No MMA may still be writing tensor memory when it is freed.
+      mma_commit(&bars->drain_s);
+      mbar_wait_drain(&bars->drain_s, 0, st.timeout_ns);
+    }
+  } else if (warp == 11) {
+    // ------------------------------------------------------ P V issuer
+    if (lane == 0) {
+      constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
       Cursor pc;
       pc.init(args, nt, n_items);
-      for (int t = 0; ok && pc.valid; ++t, pc.next(args)) {
+      for (int t = 0; pc.valid; ++t, pc.next(args)) {
         const int buf = t % kSBuf;
         if (!mbar_wait(&bars->p_full[buf], (t / kSBuf) & 1, st, abort_flag, kSitePFull)) break;
         const int v = t % SV;
@@ -272,34 +300,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t va = sV + v * L::kTile;
 #pragma unroll
         for (int k16 = 0; k16 < kBN / 16; ++k16)
-          mma_bf16_ts(tO, tmem + buf * 128 + k16 * 8, desc_mnmajor(va, k16, kBlockBytes), idO,
+          mma_bf16_ts(tO, tmem + 256 + buf * 64 + k16 * 8, desc_mnmajor(va, k16, kBlockBytes), idO,
                       (pc.j > 0 || k16 > 0) ? 1u : 0u);
         mma_commit(&bars->o_done[t & 1]);
         mma_commit(&bars->v_empty[v]);
-        // S_{t+2} goes into the buffer that held P_{t-1}: P V_{t-1} must be done.
-        if (t >= 1 && !mbar_wait(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteOPrev))
-          break;
-        tc_fence_after();
-        if (!issue_s()) break;
       }
-      // No MMA may still be writing tensor memory when it is freed.
-      mma_commit(&bars->drain);
-      mbar_wait_drain(&bars->drain, 0, st.timeout_ns);
+      mma_commit(&bars->drain_pv);
+      mbar_wait_drain(&bars->drain_pv, 0, st.timeout_ns);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 9) {
     // ------------------------------------------------------ softmax
+    const int g = (warp - 2) >> 2;               // softmax group 0 or 1: owns tiles t with t % 2 == g
     const int quad = warp & 3;
     const int r = quad * 32 + lane;              // row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    float* mref = reinterpret_cast<float*>(smem + L::kMref);   // [tile parity][row]
+    float* lxb = reinterpret_cast<float*>(smem + L::kLx);      // [item parity][row]
     const float sl2 = args.scale_log2;
     const uint64_t sl2x2 = f2pack(sl2, sl2);
-    float m_run = -INFINITY;                     // reference max of scale*log2(e)*s (may lag by <= 2^8)
-    float l_run = 0.f;                           // running denominator relative to m_run
+    float m_g = -INFINITY;                       // reference max this group's row sum is relative to
+    float l_g = 0.f;                             // this group's part of the row sum
+    int my_item = -1;                            // item the group's (l_g, m_g) belong to
+    int n_multi = 0;                             // items with >= 2 tiles completed so far
     Cursor c;
     c.init(args, nt, n_items);
     for (int t = 0; c.valid; ++t, c.next(args)) {
+      const int j = c.j, n = c.it.n;
+      const int n_multi_before = n_multi;
+      const int multi_slot = n_multi & 1;
+      if (j == n - 1 && n >= 2) ++n_multi;
+      if ((t & 1) != g) continue;                // the other group's tile
       const int buf = t % kSBuf;
-      const int j = c.j;
       const int row = c.it.qt * kBM + r;
       const uint32_t tS = tmem + buf * 128 + lane_off;
       if (!mbar_wait_warp(&bars->s_full[buf], (t / kSBuf) & 1, st, abort_flag, kSiteSFull)) break;
@@ -310,6 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
 #pragma unroll
       for (int q = 0; q < 4; ++q) reg_fence(sr[q]);
+      tc_fence_before();
+      mbar_arrive(&bars->s_free[buf]);   // the MMA may compute S_{t+2} into this buffer now
 
       const int key0 = j * kBN;
       if ((key0 + kBN > N) || (args.causal && j == c.it.qt)) {
@@ -320,7 +353,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (q * 32 + e >= lim) sr[q][e] = __float_as_uint(-INFINITY);
       }
-      // Row max: four independent three-input max chains.
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -333,22 +365,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-      if (j == 0) {
-        m_run = -INFINITY;
-        l_run = 0.f;
+      // Reference max after the previous tile (owned by the other group).  The
+      // wait also happens at an item's first tile, where the value is unused:
+      // it keeps the two groups' hand-offs strictly alternating, so no hand
+      // barrier can run two phases ahead of its waiter.
+      float m_prev = -INFINITY;
+      if (t > 0) {
+        if (!mbar_wait_warp(&bars->hand[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteHand)) break;
+        if (j > 0) m_prev = mref[((t - 1) & 1) * 128 + r];
       }
-      const bool need = (j == 0) || (m_cand > m_run + kRescaleThreshold);
-      const float m_new = need ? m_cand : m_run;
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = need ? ex2(m_run - m_use) : 1.f;
-      m_run = m_new;
+      const bool need = (j == 0) || (m_cand > m_prev + kRescaleThreshold);
+      const float m_new = need ? m_cand : m_prev;
+      // Hand the reference on to the owner of tile t+1 right away.
+      mref[(t & 1) * 128 + r] = m_new;
+      mbar_arrive(&bars->hand[t & 1]);
 
-      // P = 2^(s*sl2 - m) in fp32 pairs; row sum in four packed accumulators.
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      if (my_item != c.item) {
+        my_item = c.item;
+        l_g = 0.f;
+      } else if (m_g != m_new) {
+        l_g *= ex2(m_g - m_use);
+      }
+      m_g = m_new;
+
+      // P = 2^(s*sl2 - m), 32 keys at a time, into probability buffer t % 2
+      // once P V_{t-2} has consumed it.
+      if (t >= 2 && !mbar_wait_warp(&bars->o_done[t & 1], ((t >> 1) - 1) & 1, st, abort_flag, kSitePPrev)) break;
+      tc_fence_after();
+      const uint32_t tP = tmem + 256 + buf * 64 + lane_off;
       const uint64_t negm = f2pack(-m_use, -m_use);
       uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
-      uint32_t pk[64];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
+        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           uint64_t x[4];
@@ -360,27 +410,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo = ex2(lo);
             hi = ex2(hi);
             x[u] = f2pack(lo, hi);
-            pk[(q * 32 + e) / 2 + u] = cvt_bf16x2(lo, hi);
+            pk[e / 2 + u] = cvt_bf16x2(lo, hi);
           }
           acc0 = fadd2(acc0, x[0]);
           acc1 = fadd2(acc1, x[1]);
           acc2 = fadd2(acc2, x[2]);
           acc3 = fadd2(acc3, x[3]);
         }
+        tmem_st16(tP + q * 16, pk);
       }
-      float a0, a1, b0, b1;
+      float a0, a1;
       f2unpack(fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3)), a0, a1);
-      l_run = l_run * alpha + (a0 + a1);
-      (void)b0;
-      (void)b1;
-
-      // P (bf16) over the first 64 columns of this tile's score buffer.
-      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      l_g += a0 + a1;
 
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O holds rows relative to the old reference max: rescale it once
+        // O holds rows relative to the previous reference: rescale it once
         // P V of the previous tile has landed.
+        const float alpha = need ? ex2(m_prev - m_use) : 1.f;
         if (!mbar_wait_warp(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteORescale)) break;
         tc_fence_after();
         const uint64_t al2 = f2pack(alpha, alpha);
@@ -404,8 +450,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->p_full[buf]);
 
-      if (j == c.it.n - 1) {
+      if (j == n - 2) {
+        // The other group owns the item's last tile: hand it this group's
+        // row-sum part, relative to m_new (which it reads back as m_prev).
+        lxb[multi_slot * 128 + r] = l_g;
+        mbar_arrive(&bars->lx[multi_slot]);
+      }
+      if (j == n - 1) {
         // ------------------------------------------------ epilogue of the item
+        float l_tot = l_g;
+        if (n >= 2) {
+          if (!mbar_wait_warp(&bars->lx[multi_slot], (n_multi_before >> 1) & 1, st, abort_flag, kSiteLx)) break;
+          l_tot += lxb[multi_slot * 128 + r] * ex2(m_prev - m_use);
+        }
         if (!mbar_wait_warp(&bars->o_done[t & 1], (t >> 1) & 1, st, abort_flag, kSiteOLast)) break;
         tc_fence_after();
         uint32_t o[D / 32][32];
@@ -416,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < D / 32; ++q) reg_fence(o[q]);
         tc_fence_before();
         mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
-        const float inv_l = 1.f / l_run;
+        const float inv_l = 1.f / l_tot;
         const size_t head = (size_t)c.it.b * args.Hq + c.it.h;
         if (row < N) {
           __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.o) + (head * N + (size_t)row) * D;
@@ -432,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint4*>(orow + q * 32 + v * 8) = w;
             }
           }
-          args.lse[head * N + row] = (m_run + __log2f(l_run)) * 0.69314718055994530942f;
+          args.lse[head * N + row] = (m_new + __log2f(l_tot)) * 0.69314718055994530942f;
         }
       }
     }
@@ -453,14 +510,14 @@ template <int D>
 static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const FwdArgs& a, const DevStatus& st, int num_sms, cudaStream_t stream) {
   using L = FwdCfg<D>;
-  static_assert(L::kAlloc <= 232448, "shared memory budget");
+  static_assert(L::kBytes <= 232448, "shared memory budget");
   static_assert(sizeof(Bars) <= 512, "barrier block");
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const long long nt = (a.N + kBM - 1) / kBM;
   const long long items = nt * a.Hq * a.B;
   const int grid = (int)(items < num_sms ? items : num_sms);
-  fa_fwd_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, a, st);
+  fa_fwd_kernel<D><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, a, st);
   return cudaGetLastError();
 }
 

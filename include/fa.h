@@ -162,6 +162,13 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
                          int causal, float scale, void* stream);
 
+/*
+ * Text of the most recent CUDA runtime error behind an FA_ERR_LAUNCH or
+ * FA_ERR_CUDA status returned on the calling thread ("no error" if none).
+ * Static string, never NULL.
+ */
+const char* fa_last_cuda_error(void);
+
 /* Library ABI version (major * 100 + minor). */
 int fa_version(void);
 
