@@ -172,6 +172,20 @@ fa_status tmap_bf16(CUtensorMap* m, const void* base, int B, int H, int N, int d
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_LAUNCH;
 }
 
+// fp32 dQ accumulator [B*Hq, N, d] viewed as {d, N, B*Hq} with a {32, 128, 1}
+// box and 128-byte swizzle, the target of the tiled TMA reduce-add.
+fa_status tmap_dq_accum(CUtensorMap* m, void* base, int B, int Hq, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)B * Hq};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_LAUNCH;
+}
+
+
 
 
 fa_status validate_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B,
@@ -286,13 +300,14 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
   FA_TRY(validate_dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
   DeviceState* ds = nullptr;
   FA_TRY(device_state(&ds));
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  const WsLayout w = ws_layout(B, Hq, N, d);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
   FA_TRY(tmap_bf16(&tq, q, B, Hq, N, d));
   FA_TRY(tmap_bf16(&tk, k, B, Hkv, N, d));
   FA_TRY(tmap_bf16(&tv, v, B, Hkv, N, d));
   FA_TRY(tmap_bf16(&tdo, dO, B, Hq, N, d));
-  const WsLayout w = ws_layout(B, Hq, N, d);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  FA_TRY(tmap_dq_accum(&tdq, ws + w.dq_off, B, Hq, N, d));
   fa::BwdArgs a;
   a.lse2 = reinterpret_cast<const float*>(ws + w.lse2_off);
   a.drow = reinterpret_cast<const float*>(ws + w.dr_off);
@@ -306,7 +321,8 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
   a.causal = causal;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_status(fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, a, dev_status(ds), static_cast<cudaStream_t>(stream)));
+  return launch_status(
+      fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, tdq, a, dev_status(ds), static_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_bwd_dq_convert(void* dq, int B, int Hq, int Hkv, int N, int d, float scale, const void* workspace,

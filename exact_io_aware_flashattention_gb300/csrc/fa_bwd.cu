@@ -16,7 +16,7 @@
 //      partial is added into the fp32 accumulator (the separate dQ reduction).
 //   3. dq_convert: dQ = bf16(scale * accumulator).
 //
-// dkdv CTA layout (320 threads):
+// dkdv CTA layout (352 threads):
 //   warp 0      TMA producer: K, V once; per item Q_i, dO_i (2 slots each) and
 //               the item's 128 LSE / D values (bulk copies, 2 slots)
 //   warp 1      TMEM allocator and MMA issuer
@@ -24,15 +24,18 @@
 //               of a group owns key row t (TMEM lane t) for S^T, dP^T, dK, dV
 //               and query row t for the dQ partial; group g handles query
 //               columns [64g, 64g+64) and head-dim columns [g d/2, (g+1) d/2).
-// Tensor memory: S^T at columns 0-127 (P^T, bf16, is written back over the
-// group's own columns: 0-31 and 64-95) and read there by the dV MMA;
+//   warp 10     dQ store: adds the staged dQ partials into the fp32
+//               accumulator with TMA reduce-adds and returns the staging slots
+// Tensor memory: S^T at columns 0-127; P^T (bf16) is written back over the
+// group's own columns 0-31 / 64-95 and read there by the dV MMA, dS^T (bf16)
+// over 32-63 / 96-127 and read there by the dK MMA;
 // dP^T at 128-255, reused for the dQ partial; dV at 256, dK at 256 + d.
-// dS^T (bf16) goes to one shared-memory tile read by both the dK MMA
-// (K-major) and the dQ MMA (as dS, MN-major).
+// dS^T (bf16) also goes to a shared-memory tile, read by the dQ MMA as dS
+// (MN-major).
 //
 // Tensor pipe order per item t:  S_t, dP_t, dV_t, dK_t, dQ_t, S_{t+1}, ...
-// S_{t+1} waits for dV_t (it overwrites P^T_t); dP_{t+1} waits until the dQ
-// partial of item t has been read out of the same columns.
+// S_{t+1} waits for dK_t (it overwrites P^T_t and dS^T_t); dP_{t+1} waits until
+// the dQ partial of item t has been read out of the same columns.
 #include "fa_internal.h"
 #include "sm103a.cuh"
 
@@ -41,7 +44,7 @@ namespace fa {
 namespace {
 
 constexpr int kT = 128;             // rows per query tile and per key tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr uint32_t kBlockBytes = 128u * 128u;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -61,13 +64,14 @@ struct BwdSmem {
 
 enum : int {
   kSiteKV = 11, kSiteQEmpty, kSiteDoEmpty, kSiteLdEmpty, kSiteQFull, kSiteDvDone, kSiteDoFull, kSiteDqEmpty,
-  kSitePFull, kSiteDsFull, kSiteLdFull, kSiteSFull, kSiteDpFull, kSiteDqFull, kSiteDkvDone
+  kSitePFull, kSiteDsFull, kSiteLdFull, kSiteSFull, kSiteDpFull, kSiteDqFull, kSiteDkvDone, kSiteStFull, kSiteDkDone
 };
 
 struct Bars {
   uint64_t kv_full;
   uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2], ld_full[2], ld_empty[2];
-  uint64_t s_full, dp_full, p_full, dv_done, ds_full, dq_full, dq_empty, dkv_done, drain;
+  uint64_t s_full, dp_full, p_full, dv_done, ds_full, dk_done, dq_full, dq_empty, dkv_done, drain;
+  uint64_t st_full[2][2];   // [slot][group]: the group's dQ partial of the slot's item is staged
   uint32_t tmem_base;
   int abort;
 };
@@ -83,10 +87,11 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                       const BwdArgs args, const DevStatus st) {
+                       const __grid_constant__ CUtensorMap tmDQ, const BwdArgs args, const DevStatus st) {
   using L = BwdSmem<D>;
   constexpr int kAtoms = D / 64;
   constexpr int kHalfD = D / 2;
+  constexpr int kPasses = kHalfD / 32;   // 32-column dQ staging passes per group
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBar);
   volatile int* abort_flag = &bars->abort;
@@ -115,17 +120,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->kv_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->q_full[s], 1);
-      mbar_init(&bars->q_empty[s], 1);
+      mbar_init(&bars->q_empty[s], 2);   // dK/dQ MMAs done + dQ staging read by TMA
       mbar_init(&bars->do_full[s], 1);
-      mbar_init(&bars->do_empty[s], 1);
+      mbar_init(&bars->do_empty[s], 2);  // dP/dV MMAs done + dQ staging read by TMA
       mbar_init(&bars->ld_full[s], 1);
       mbar_init(&bars->ld_empty[s], 256);
+      for (int g = 0; g < 2; ++g) mbar_init(&bars->st_full[s][g], 128);
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_full, 256);
     mbar_init(&bars->dv_done, 1);
     mbar_init(&bars->ds_full, 256);
+    mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_empty, 256);
     mbar_init(&bars->dkv_done, 1);
@@ -137,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmDQ);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -154,6 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sDO = smem_u32(smem + L::kDO);
   const uint32_t sDS = smem_u32(smem + L::kDS);
   const int ntp = nt * kT;                       // padded rows per head of the LSE / D arrays
+  // Staging block of the dQ partial of (slot, group g, 32-column pass q): for
+  // d = 128 pass 0 uses block g of the slot's dO tile and pass 1 block g of
+  // its Q tile; for d = 64 (one 16 KB block per tile) group 0 uses the dO
+  // tile and group 1 the Q tile.
+  auto stage_addr = [&](int slot, int g, int q) -> uint32_t {
+    if (kPasses == 2) return (q == 0 ? sDO : sQ) + slot * L::kTile + g * kBlockBytes;
+    return (g == 0 ? sDO : sQ) + slot * L::kTile;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -164,17 +180,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(smem + L::kV + a * kBlockBytes, &tmV, &bars->kv_full, a * 64, j * kT, kvh, b);
       }
       int n_ld[2] = {0, 0}, n_q[2] = {0, 0}, n_do[2] = {0, 0};   // copies issued per slot
-      for (int t = 0; t < n_items; ++t) {
-        const int h = kvh * G + t / nqi;
-        const int i = i0 + t % nqi;
-        const int slot = t & 1;
-        const uint32_t ph = ((t >> 1) - 1) & 1;   // phase of this slot's previous use
-        if (t >= 2 && !mbar_wait(&bars->ld_empty[slot], ph, st, abort_flag, kSiteLdEmpty)) break;
+      // LSE*log2(e) and D of item u (512 bytes each) go to slot u % 2; they are
+      // issued one item ahead of that item's Q / dO tiles.
+      auto issue_ld = [&](int u) -> bool {
+        if (u >= n_items) return true;
+        const int slot = u & 1;
+        if (u >= 2 && !mbar_wait(&bars->ld_empty[slot], ((u >> 1) - 1) & 1, st, abort_flag, kSiteLdEmpty))
+          return false;
+        const int h = kvh * G + u / nqi;
+        const int i = i0 + u % nqi;
         const size_t roff = ((size_t)b * args.Hq + h) * ntp + (size_t)i * kT;
         mbar_arrive_expect_tx(&bars->ld_full[slot], 1024u);
         bulk_load(smem + L::kLse + slot * 512, args.lse2 + roff, 512u, &bars->ld_full[slot]);
         bulk_load(smem + L::kDr + slot * 512, args.drow + roff, 512u, &bars->ld_full[slot]);
         ++n_ld[slot];
+        return true;
+      };
+      bool pok = issue_ld(0);
+      for (int t = 0; pok && t < n_items; ++t) {
+        const int h = kvh * G + t / nqi;
+        const int i = i0 + t % nqi;
+        const int slot = t & 1;
+        const uint32_t ph = ((t >> 1) - 1) & 1;   // phase of this slot's previous use
         if (t >= 2 && !mbar_wait(&bars->q_empty[slot], ph, st, abort_flag, kSiteQEmpty)) break;
         mbar_arrive_expect_tx(&bars->q_full[slot], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
@@ -187,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(smem + L::kDO + slot * L::kTile + a * kBlockBytes, &tmDO, &bars->do_full[slot], a * 64,
                       i * kT, h, b);
         ++n_do[slot];
+        pok = issue_ld(t + 1);
       }
       // Every copy issued must have landed before the CTA may exit.
       mbar_wait_drain(&bars->kv_full, 0, st.timeout_ns);
@@ -210,7 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t pph = (t - 1) & 1;    // previous item's phase
         const uint32_t qa = sQ + slot * L::kTile, da = sDO + slot * L::kTile;
         if (!mbar_wait(&bars->q_full[slot], sph, st, abort_flag, kSiteQFull)) break;
-        if (t > 0 && !mbar_wait(&bars->dv_done, pph, st, abort_flag, kSiteDvDone)) break;
+        // S_{t+1} overwrites the score region, which holds P^T_t (read by dV_t)
+        // and dS^T_t (read by dK_t); dK_t is the later of the two.
+        if (t > 0 && !mbar_wait(&bars->dk_done, pph, st, abort_flag, kSiteDkDone)) break;
         tc_fence_after();
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
@@ -234,10 +264,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars->do_empty[slot]);
         if (!mbar_wait(&bars->ds_full, ph, st, abort_flag, kSiteDsFull)) break;
         tc_fence_after();
+        // dS^T for query columns 16*k16.. lives at column (k16/4)*64 + 32 + (k16%4)*8.
 #pragma unroll
         for (int k16 = 0; k16 < kT / 16; ++k16)
-          mma_bf16_ss(tDK, desc_kmajor(sDS, k16, kBlockBytes), desc_mnmajor(qa, k16, kBlockBytes), idKM,
+          mma_bf16_ts(tDK, tS + (k16 >> 2) * 64 + 32 + (k16 & 3) * 8, desc_mnmajor(qa, k16, kBlockBytes), idKM,
                       (t > 0 || k16 > 0) ? 1u : 0u);
+        mma_commit(&bars->dk_done);
 #pragma unroll
         for (int k16 = 0; k16 < kT / 16; ++k16)
           mma_bf16_ss(tDP, desc_mnmajor(sDS, k16, kBlockBytes), desc_mnmajor(sK, k16, kBlockBytes), idMM,
@@ -249,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, st.timeout_ns);
     }
-  } else {
+  } else if (warp < 10) {
     // ------------------------------------------------------------ compute
     const int g = (warp - 2) >> 2;                 // warpgroup 0 or 1
     const int quad = warp & 3;
@@ -263,8 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < n_items; ++t) {
       const int slot = t & 1;
       const uint32_t ph = t & 1;
-      const int h = kvh * G + t / nqi;
       const int i = i0 + t % nqi;
+      auto dq_stage = [&](int q) { return stage_addr(slot, g, q); };
       const float* lse_t = reinterpret_cast<const float*>(smem + L::kLse + slot * 512) + c0;
       const float* dr_t = reinterpret_cast<const float*>(smem + L::kDr + slot * 512) + c0;
       if (!mbar_wait_warp(&bars->ld_full[slot], (t >> 1) & 1, st, abort_flag, kSiteLdFull)) { ok = false; break; }
@@ -335,38 +367,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           ds[(col >> 1) + 1] = cvt_bf16x2(a2, a3);
         }
       }
-      // dS^T row -> this group's 64-column block of the shared tile.
+      // dS^T row -> tensor memory (this group's spare score columns, the A
+      // operand of dK) and this group's 64-column block of the shared tile
+      // (the A operand of dQ).
+      tmem_st32(tS + lane_off + c0 + 32, ds);
 #pragma unroll
       for (int c16 = 0; c16 < 8; ++c16)
         st_shared_v4(sDS + g * kBlockBytes + swz128(r, c16), ds[c16 * 4], ds[c16 * 4 + 1], ds[c16 * 4 + 2],
                      ds[c16 * 4 + 3]);
       fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->ds_full);
       mbar_arrive(&bars->ld_empty[slot]);
 
       if (!mbar_wait_warp(&bars->dq_full, ph, st, abort_flag, kSiteDqFull)) { ok = false; break; }
       tc_fence_after();
-      // dQ partial row r (a query) x this group's head-dim columns.
-      const int qrow = i * kT + r;
-      const size_t head = (size_t)b * args.Hq + h;
-      float* dq_row = args.dq_accum + (head * N + (size_t)qrow) * D + g * kHalfD;
+      // dQ partial row r (a query) x this group's head-dim columns: read it out
+      // of tensor memory (freeing those columns for dP^T of the next item) and
+      // stage it 32 columns at a time, 128-byte swizzled, in this item's dO
+      // and Q tiles -- free now: their last readers, the dV and dK MMAs, have
+      // completed.  The store warp adds the staged blocks into the fp32
+      // accumulator.
+      {
+        uint32_t v[kPasses][32];
 #pragma unroll
-      for (int q = 0; q < kHalfD / 32; ++q) {
-        uint32_t v[32];
-        tmem_ld32(tDP + lane_off + g * kHalfD + q * 32, v);
+        for (int q = 0; q < kPasses; ++q) tmem_ld32(tDP + lane_off + g * kHalfD + q * 32, v[q]);
         tmem_wait_ld();
-        reg_fence(v);
-        if (qrow < N) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            atomicAdd(reinterpret_cast<float4*>(dq_row + q * 32 + e),
-                      make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                                  __uint_as_float(v[e + 3])));
+        for (int q = 0; q < kPasses; ++q) reg_fence(v[q]);
+        tc_fence_before();
+        mbar_arrive(&bars->dq_empty);
+#pragma unroll
+        for (int q = 0; q < kPasses; ++q) {
+          const uint32_t stage = dq_stage(q);
+#pragma unroll
+          for (int c16 = 0; c16 < 8; ++c16)
+            st_shared_v4(stage + swz128(r, c16), v[q][c16 * 4], v[q][c16 * 4 + 1], v[q][c16 * 4 + 2],
+                         v[q][c16 * 4 + 3]);
         }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->st_full[slot][g]);
       }
-      tc_fence_before();
-      mbar_arrive(&bars->dq_empty);
     }
 
     if (ok && mbar_wait_warp(&bars->dkv_done, 0, st, abort_flag, kSiteDkvDone)) {
@@ -396,6 +438,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ store
+    // Per item: wait until both groups have staged their dQ partial, add each
+    // 128 x 32 fp32 block into the accumulator with one tiled TMA reduce-add
+    // (rows past N are clipped by the tensor map), and hand the item's dO and
+    // Q slots back to the producer once TMA has read the staging.  Waiting
+    // for those reads here keeps them off the compute warps.
+    if (lane == 0) {
+      for (int t = 0; t < n_items; ++t) {
+        const int slot = t & 1;
+        const int head = b * args.Hq + kvh * G + t / nqi;
+        const int i = i0 + t % nqi;
+        bool sok = true;
+        for (int g = 0; sok && g < 2; ++g) {
+          sok = mbar_wait(&bars->st_full[slot][g], (t >> 1) & 1, st, abort_flag, kSiteStFull);
+          if (!sok) break;
+#pragma unroll
+          for (int q = 0; q < kPasses; ++q)
+            tma_reduce_add_3d(&tmDQ, stage_addr(slot, g, q), g * kHalfD + q * 32, i * kT, head);
+        }
+        bulk_commit_group();
+        if (!sok) break;
+        bulk_wait_read_all();
+        mbar_arrive(&bars->do_empty[slot]);
+        mbar_arrive(&bars->q_empty[slot]);
+      }
+      // The additions must have landed before the kernel is complete.
+      bulk_wait_all();
     }
   }
 
@@ -473,7 +544,8 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float4* __
 
 template <int D>
 static cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                 const CUtensorMap& tdo, const BwdArgs& a, const DevStatus& st, cudaStream_t stream) {
+                                 const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, const DevStatus& st,
+                                 cudaStream_t stream) {
   using L = BwdSmem<D>;
   static_assert(L::kBytes <= 232448, "shared memory budget");
   static_assert(sizeof(Bars) <= 256, "barrier block");
@@ -482,14 +554,15 @@ static cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, c
   if (e != cudaSuccess) return e;
   const int nt = (a.N + kT - 1) / kT;
   dim3 grid(a.Hkv, a.B, nt);
-  fa_bwd_dkdv_kernel<D><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, a, st);
+  fa_bwd_dkdv_kernel<D><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, a, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdArgs& a, const DevStatus& st, cudaStream_t stream) {
-  if (d == 64) return launch_dkdv_d<64>(tq, tk, tv, tdo, a, st, stream);
-  return launch_dkdv_d<128>(tq, tk, tv, tdo, a, st, stream);
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, const DevStatus& st,
+                            cudaStream_t stream) {
+  if (d == 64) return launch_dkdv_d<64>(tq, tk, tv, tdo, tdq, a, st, stream);
+  return launch_dkdv_d<128>(tq, tk, tv, tdo, tdq, a, st, stream);
 }
 
 static int grid_for(long long work_items, int num_sms) {

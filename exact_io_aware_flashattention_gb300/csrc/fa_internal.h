@@ -37,7 +37,8 @@ cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dO, const fl
                                   float* dq_accum, long long heads, int N, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdArgs& a, const DevStatus& st, cudaStream_t stream);
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, const DevStatus& st,
+                            cudaStream_t stream);
 
 cudaError_t launch_bwd_dq_convert(const float* dq_accum, void* dq, float scale, long long n, int num_sms,
                                   cudaStream_t stream);

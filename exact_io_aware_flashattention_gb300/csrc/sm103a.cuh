@@ -106,13 +106,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
-// Warp-collective form: every lane waits, and the warp proceeds only if all
-// lanes succeeded, so lanes never split across a later .sync.aligned
-// instruction or warp vote.
+// Warp-collective form: lane 0 waits (bounded), the other lanes wait for it
+// at a warp barrier, and the warp proceeds only if the wait succeeded, so
+// lanes never split across a later .sync.aligned instruction or warp vote.
+// (One suspended waiter per warp instead of 32.)  The warp barrier orders
+// lane 0's acquire of the mbarrier before the other lanes' later accesses.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const DevStatus& st,
                                                volatile int* abort, int site) {
-  const bool ok = mbar_wait(bar, parity, st, abort, site);
-  return __all_sync(0xffffffffu, ok);
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, st, abort, site) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
 }
 
 // Bounded wait that ignores the abort flag (used to drain in-flight copies).
@@ -161,6 +166,30 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
 }
+
+// Tiled 3-D reduce-add of a shared-memory box into global memory (the tensor
+// map's element type and reduction), tracked by this thread's bulk group.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t ssrc, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(ssrc)
+      : "memory");
+}
+
+// Bulk (non-tensor) reduce-add of `bytes` fp32 values from shared to global
+// memory, tracked by this thread's bulk async-group.  Both addresses 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's bulk groups have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until this thread's bulk groups have fully completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory
