@@ -163,12 +163,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sDS = smem_u32(smem + L::kDS);
   const int ntp = nt * kT;                       // padded rows per head of the LSE / D arrays
   // Staging block of the dQ partial of (slot, group g, 32-column pass q): for
-  // d = 128 pass 0 uses block g of the slot's dO tile and pass 1 block g of
-  // its Q tile; for d = 64 (one 16 KB block per tile) group 0 uses the dO
-  // tile and group 1 the Q tile.
+  // d = 128 pass 0 uses block g of the slot's Q tile and pass 1 block g of
+  // its dO tile; for d = 64 (one 16 KB block per tile) group 0 uses the Q
+  // tile and group 1 the dO tile.  The Q-tile blocks are added first, so the
+  // Q slot, needed first by the next item that uses it, is returned first.
+  auto stage_in_q = [&](int g, int q) -> bool { return kPasses == 2 ? q == 0 : g == 0; };
   auto stage_addr = [&](int slot, int g, int q) -> uint32_t {
-    if (kPasses == 2) return (q == 0 ? sDO : sQ) + slot * L::kTile + g * kBlockBytes;
-    return (g == 0 ? sDO : sQ) + slot * L::kTile;
+    return (stage_in_q(g, q) ? sQ : sDO) + slot * L::kTile + (kPasses == 2 ? g * kBlockBytes : 0u);
   };
 
   if (warp == 0) {
@@ -451,19 +452,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot = t & 1;
         const int head = b * args.Hq + kvh * G + t / nqi;
         const int i = i0 + t % nqi;
-        bool sok = true;
-        for (int g = 0; sok && g < 2; ++g) {
-          sok = mbar_wait(&bars->st_full[slot][g], (t >> 1) & 1, st, abort_flag, kSiteStFull);
-          if (!sok) break;
+        if (!mbar_wait(&bars->st_full[slot][0], (t >> 1) & 1, st, abort_flag, kSiteStFull)) break;
+        if (!mbar_wait(&bars->st_full[slot][1], (t >> 1) & 1, st, abort_flag, kSiteStFull)) break;
 #pragma unroll
-          for (int q = 0; q < kPasses; ++q)
-            tma_reduce_add_3d(&tmDQ, stage_addr(slot, g, q), g * kHalfD + q * 32, i * kT, head);
+        for (int in_q = 1; in_q >= 0; --in_q) {
+#pragma unroll
+          for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int q = 0; q < kPasses; ++q)
+              if (stage_in_q(g, q) == (in_q != 0))
+                tma_reduce_add_3d(&tmDQ, stage_addr(slot, g, q), g * kHalfD + q * 32, i * kT, head);
+          bulk_commit_group();
         }
-        bulk_commit_group();
-        if (!sok) break;
-        bulk_wait_read_all();
-        mbar_arrive(&bars->do_empty[slot]);
+        bulk_wait_read<1>();
         mbar_arrive(&bars->q_empty[slot]);
+        bulk_wait_read<0>();
+        mbar_arrive(&bars->do_empty[slot]);
       }
       // The additions must have landed before the kernel is complete.
       bulk_wait_all();
