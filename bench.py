@@ -75,19 +75,27 @@ def bf16_peak():
         return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement)"
 
 
-def kernel_source_hash():
+# Source files each timed kernel is compiled from; a committed ncu figure is
+# used only while these files are unchanged.
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ("fa_fwd.cu", "fa_internal.h", "sm103a.cuh"),
+    "fa_bwd_dkdv_kernel": ("fa_bwd.cu", "fa_internal.h", "sm103a.cuh"),
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_io_aware_flashattention_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel, workload, src_hash):
+def ncu_traffic(kernel, workload):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    if there is none for this workload or the kernel sources changed since."""
+    if there is none for this workload or the kernel's sources changed since."""
+    src_hash = kernel_source_hash(kernel)
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(p) as f:
@@ -349,7 +357,7 @@ def run_ours(args, w):
     else:
         dom, dom_flops, dom_ms = "fa_fwd_kernel", w.fwd_flops, fwd_avg
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    src_hash = kernel_source_hash()
+    src_hash = {k: kernel_source_hash(k) for k in KERNEL_SOURCES}
 
     # ---------------- e2e through host buffers (pinned), copies inside the timed region
     e2e = None
@@ -406,7 +414,7 @@ def run_ours(args, w):
                     "ms_dq_convert": statistics.mean(conv_ms)},
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
-                         "traffic": ncu_traffic(dom, w.name, src_hash),
+                         "traffic": ncu_traffic(dom, w.name),
                          "algorithmic_flops_per_launch": dom_flops},
             "cpu_baseline": cpu,
             "e2e": e2e,
