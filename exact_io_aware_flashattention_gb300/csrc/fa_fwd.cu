@@ -13,7 +13,7 @@
 // units), which keeps every exponent <= 2^8 and skips most rescales.
 //
 // Persistent kernel: one CTA per SM walks work items (query tile, head,
-// batch), heaviest causal tiles first.  CTA layout (384 threads):
+// batch), heaviest causal tiles first, dealt to the CTAs in snake order.  CTA layout (384 threads):
 //   warp 0      TMA producer for Q (2 slots) and K (ring of kStagesK)
 //   warp 1      TMEM allocator; one thread issues the S = Q K^T MMAs
 //   warp 11     one thread issues the O += P V MMAs.  The two issuers touch
@@ -107,6 +107,14 @@ __device__ __forceinline__ Item decode_item(int idx, const FwdArgs& a, int nt) {
   return it;
 }
 
+// Item of this CTA in round k: rounds alternate direction over the CTAs, so
+// the CTA that drew a heavy item in one round draws a light one in the next
+// (with heaviest-first ranks this balances causal work to within a few %).
+__device__ __forceinline__ int item_of_round(int k) {
+  const int g = gridDim.x;
+  return k * g + ((k & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x);
+}
+
 // Walks this CTA's (item, key tile) sequence.
 struct Cursor {
   int item, li, j, n_items, nt;
@@ -115,17 +123,17 @@ struct Cursor {
   __device__ __forceinline__ void init(const FwdArgs& a, int nt_, int n_items_) {
     nt = nt_;
     n_items = n_items_;
-    item = blockIdx.x;
     li = 0;
     j = 0;
+    item = item_of_round(0);
     valid = item < n_items;
     if (valid) it = decode_item(item, a, nt);
   }
   __device__ __forceinline__ void next(const FwdArgs& a) {
     if (++j == it.n) {
       j = 0;
-      item += gridDim.x;
       ++li;
+      item = item_of_round(li);
       valid = item < n_items;
       if (valid) it = decode_item(item, a, nt);
     }
@@ -207,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kt = 0, li = 0;
       int q_issued[2] = {0, 0};
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++li) {
+      for (int item = item_of_round(0); ok && item < n_items; item = item_of_round(++li)) {
         const Item it = decode_item(item, args, nt);
         const int slot = li & 1;
         if (li >= 2 && !mbar_wait(&bars->q_empty[slot], ((li >> 1) - 1) & 1, st, abort_flag, kSiteQEmpty)) break;
@@ -238,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int vt = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      for (int round = 0, item = item_of_round(0); ok && item < n_items; item = item_of_round(++round)) {
         const Item it = decode_item(item, args, nt);
         for (int j = 0; j < it.n; ++j, ++vt) {
           const int s = vt % SV, r = vt / SV;
