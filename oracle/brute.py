@@ -14,10 +14,16 @@ def _dot(a, b):
     return sum(x * y for x, y in zip(a, b))
 
 
-def forward(q, k, v, causal: bool, scale: float):
+def _keys(i, N, Nk, causal, window):
+    # Query row i stands at position i + Nk - N (the last N of Nk positions).
+    p = i + Nk - N
+    return [j for j in range(Nk) if (not causal or (j <= p and (window == 0 or j > p - window)))]
+
+
+def forward(q, k, v, causal: bool, scale: float, window: int = 0):
     """Return (o, lse) as nested lists."""
     B, Hq, N, d = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
-    Hkv = len(k[0])
+    Hkv, Nk = len(k[0]), len(k[0][0])
     group = Hq // Hkv
     o = [[[[0.0] * d for _ in range(N)] for _ in range(Hq)] for _ in range(B)]
     lse = [[[0.0] * N for _ in range(Hq)] for _ in range(B)]
@@ -25,7 +31,7 @@ def forward(q, k, v, causal: bool, scale: float):
         for h in range(Hq):
             g = h // group
             for i in range(N):
-                keys = [j for j in range(N) if (not causal or j <= i)]
+                keys = _keys(i, N, Nk, causal, window)
                 s = [scale * _dot(q[b][h][i], k[b][g][j]) for j in keys]
                 m = max(s)
                 w = [math.exp(x - m) for x in s]
@@ -36,19 +42,19 @@ def forward(q, k, v, causal: bool, scale: float):
     return o, lse
 
 
-def backward(q, k, v, do, causal: bool, scale: float):
+def backward(q, k, v, do, causal: bool, scale: float, window: int = 0):
     """Return (dq, dk, dv) as nested lists, element by element."""
     B, Hq, N, d = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
-    Hkv = len(k[0])
+    Hkv, Nk = len(k[0]), len(k[0][0])
     group = Hq // Hkv
     dq = [[[[0.0] * d for _ in range(N)] for _ in range(Hq)] for _ in range(B)]
-    dk = [[[[0.0] * d for _ in range(N)] for _ in range(Hkv)] for _ in range(B)]
-    dv = [[[[0.0] * d for _ in range(N)] for _ in range(Hkv)] for _ in range(B)]
+    dk = [[[[0.0] * d for _ in range(Nk)] for _ in range(Hkv)] for _ in range(B)]
+    dv = [[[[0.0] * d for _ in range(Nk)] for _ in range(Hkv)] for _ in range(B)]
     for b in range(B):
         for h in range(Hq):
             g = h // group
             for i in range(N):
-                keys = [j for j in range(N) if (not causal or j <= i)]
+                keys = _keys(i, N, Nk, causal, window)
                 s = [scale * _dot(q[b][h][i], k[b][g][j]) for j in keys]
                 m = max(s)
                 w = [math.exp(x - m) for x in s]

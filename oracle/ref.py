@@ -9,6 +9,13 @@ b and query head h, with key/value group g(h),
     LSE_i = m_i + ln sum_j exp(S_ij - m_i)   (natural log, includes the scale)
 
 Causal [Lecture, "GPU 显存和注意力瓶颈"]: query i sees key j iff j <= i.
+With fewer query rows than keys (Nq < Nk, the decode shape: a few new
+queries against a long key/value history) query row i stands at position
+i + (Nk - Nq), the last Nq positions, and causal visibility compares key
+positions with that.  Sliding window ([ZeRO-vs-FA] "注意力瓶颈与优化路线" and
+[FA-memory] part 2 name local windows as a different visibility pattern):
+with window w >= 1 query position p sees key j iff p - w < j <= p; the window
+is only defined together with causal visibility.
 Grouped-query attention [Lecture, "减少缓存表示并验证草稿"]: Hq query heads
 share Hkv key/value heads; query head h reads kv head h // (Hq // Hkv), so
 Hkv == Hq is ordinary multi-head attention and Hkv == 1 is multi-query
@@ -33,7 +40,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = ["attention_forward", "attention_backward", "kv_head_index",
-           "visible_mask", "softmax_rows"]
+           "visible_mask", "softmax_rows", "query_positions", "merge_partials"]
 
 
 def kv_head_index(h: int, Hq: int, Hkv: int) -> int:
@@ -41,12 +48,24 @@ def kv_head_index(h: int, Hq: int, Hkv: int) -> int:
     return h // (Hq // Hkv)
 
 
-def visible_mask(rows: np.ndarray, N: int, causal: bool) -> np.ndarray:
-    """Boolean [len(rows), N]: True where query rows[r] may attend to key j."""
+def query_positions(rows: np.ndarray, Nq: int, Nk: int) -> np.ndarray:
+    """Positions of query rows among the keys: the Nq queries are the last Nq
+    positions (row i stands at i + Nk - Nq; i itself when Nq == Nk)."""
+    return np.asarray(rows) + (Nk - Nq)
+
+
+def visible_mask(pos: np.ndarray, N: int, causal: bool, window: int = 0) -> np.ndarray:
+    """Boolean [len(pos), N]: True where the query at position pos[r] may attend
+    to key j (j <= pos when causal; also j > pos - window when window > 0)."""
     cols = np.arange(N)
+    if window and not causal:
+        raise ValueError("a sliding window needs causal visibility")
     if causal:
-        return cols[None, :] <= rows[:, None]
-    return np.ones((len(rows), N), dtype=bool)
+        m = cols[None, :] <= pos[:, None]
+        if window:
+            m &= cols[None, :] > pos[:, None] - window
+        return m
+    return np.ones((len(pos), N), dtype=bool)
 
 
 def softmax_rows(s: np.ndarray):
@@ -60,21 +79,24 @@ def softmax_rows(s: np.ndarray):
     return e / den, m[:, 0], den[:, 0]
 
 
-def _check_shapes(q, k, v):
+def _check_shapes(q, k, v, causal=False):
     if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
         raise ValueError("q, k, v must be [B, H, N, d]")
-    B, Hq, N, d = q.shape
-    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != N or k.shape[3] != d:
-        raise ValueError("k and v must be [B, Hkv, N, d] matching q")
-    Hkv = k.shape[1]
+    B, Hq, Nq, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k and v must be [B, Hkv, Nk, d] matching q")
+    Hkv, Nk = k.shape[1], k.shape[2]
     if Hkv < 1 or Hq % Hkv != 0:
         raise ValueError("Hq must be a multiple of Hkv")
-    return B, Hq, Hkv, N, d
+    if causal and Nq > Nk:
+        raise ValueError("causal visibility needs Nq <= Nk")
+    return B, Hq, Hkv, Nq, Nk, d
 
 
-def _rows_of_p(q_blk, k_g, rows, N, causal, scale):
+def _rows_of_p(q_blk, k_g, rows, Nq, causal, scale, window):
+    Nk = k_g.shape[0]
     s = scale * (q_blk @ k_g.T)
-    s = np.where(visible_mask(rows, N, causal), s, -np.inf)
+    s = np.where(visible_mask(query_positions(rows, Nq, Nk), Nk, causal, window), s, -np.inf)
     return softmax_rows(s)
 
 
@@ -87,8 +109,8 @@ def _row_span(N, row_range):
     return r0, r1
 
 
-def attention_forward(q, k, v, causal: bool, scale: float, row_block: int = 512, row_range=None):
-    """O [B,Hq,N,d] and LSE [B,Hq,N] of exact attention, in fp64.
+def attention_forward(q, k, v, causal: bool, scale: float, row_block: int = 512, row_range=None, window: int = 0):
+    """O [B,Hq,Nq,d] and LSE [B,Hq,Nq] of exact attention, in fp64.
 
     ``row_range=(r0, r1)`` computes only query rows r0..r1-1 (the other rows of
     the outputs are left as NaN); each row is still the full two-pass softmax
@@ -97,7 +119,7 @@ def attention_forward(q, k, v, causal: bool, scale: float, row_block: int = 512,
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
-    B, Hq, Hkv, N, d = _check_shapes(q, k, v)
+    B, Hq, Hkv, N, Nk, d = _check_shapes(q, k, v, causal)
     lo, hi = _row_span(N, row_range)
     o = np.full((B, Hq, N, d), np.nan)
     lse = np.full((B, Hq, N), np.nan)
@@ -107,13 +129,14 @@ def attention_forward(q, k, v, causal: bool, scale: float, row_block: int = 512,
             for r0 in range(lo, hi, row_block):
                 r1 = min(hi, r0 + row_block)
                 rows = np.arange(r0, r1)
-                p, m, den = _rows_of_p(q[b, h, r0:r1], k[b, g], rows, N, causal, scale)
+                p, m, den = _rows_of_p(q[b, h, r0:r1], k[b, g], rows, N, causal, scale, window)
                 o[b, h, r0:r1] = p @ v[b, g]
                 lse[b, h, r0:r1] = m + np.log(den)
     return o, lse
 
 
-def attention_backward(q, k, v, do, causal: bool, scale: float, row_block: int = 512, row_range=None):
+def attention_backward(q, k, v, do, causal: bool, scale: float, row_block: int = 512, row_range=None,
+                       window: int = 0):
     """(dQ, dK, dV) of L = sum(dO * O) for exact attention, in fp64.
 
     ``row_range=(r0, r1)`` restricts the sum to query rows r0..r1-1: dQ rows
@@ -123,12 +146,12 @@ def attention_backward(q, k, v, do, causal: bool, scale: float, row_block: int =
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     do = np.asarray(do, dtype=np.float64)
-    B, Hq, Hkv, N, d = _check_shapes(q, k, v)
+    B, Hq, Hkv, N, Nk, d = _check_shapes(q, k, v, causal)
     if do.shape != q.shape:
         raise ValueError("dO must match q")
     dq = np.zeros((B, Hq, N, d))
-    dk = np.zeros((B, Hkv, N, d))
-    dv = np.zeros((B, Hkv, N, d))
+    dk = np.zeros((B, Hkv, Nk, d))
+    dv = np.zeros((B, Hkv, Nk, d))
     lo, hi = _row_span(N, row_range)
     for b in range(B):
         for h in range(Hq):
@@ -138,10 +161,35 @@ def attention_backward(q, k, v, do, causal: bool, scale: float, row_block: int =
                 rows = np.arange(r0, r1)
                 q_blk = q[b, h, r0:r1]
                 do_blk = do[b, h, r0:r1]
-                p, _, _ = _rows_of_p(q_blk, k[b, g], rows, N, causal, scale)
+                p, _, _ = _rows_of_p(q_blk, k[b, g], rows, N, causal, scale, window)
                 dv[b, g] += p.T @ do_blk
                 dp = do_blk @ v[b, g].T
                 ds = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
                 dq[b, h, r0:r1] = scale * (ds @ k[b, g])
                 dk[b, g] += scale * (ds.T @ q_blk)
     return dq, dk, dv
+
+
+def merge_partials(o_parts, lse_parts):
+    """Combine attention over disjoint key subsets into attention over their union.
+
+    Part s holds O_s (normalised within its keys) and LSE_s = ln sum_{j in s}
+    exp(S_ij); a part with no visible key has LSE_s = -inf and is ignored.
+    Following [Lecture] "推导 FlashAttention 的在线 softmax" -- numerator and
+    denominator carried relative to a reference maximum and rescaled by
+    exp(old - new) when that reference changes -- each part's numerator is
+    exp(LSE_s) O_s and its denominator exp(LSE_s); both are taken relative to
+    m = max_s LSE_s, summed, and divided:
+
+        O = sum_s exp(LSE_s - m) O_s / sum_s exp(LSE_s - m),
+        LSE = m + ln sum_s exp(LSE_s - m).
+
+    o_parts: [S, ..., d]; lse_parts: [S, ...].
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    m = np.max(lse_parts, axis=0)
+    w = np.exp(lse_parts - m[None])
+    den = np.sum(w, axis=0)
+    num = np.sum(np.where(w[..., None] > 0, w[..., None] * o_parts, 0.0), axis=0)
+    return num / den[..., None], m + np.log(den)

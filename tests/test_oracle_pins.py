@@ -425,7 +425,7 @@ def test_mutant_gqa_mapping_is_caught(monkeypatch):
 def test_mutant_strict_causal_is_caught(monkeypatch):
     # Query i seeing only keys j < i (itself excluded).
     monkeypatch.setattr(ref, "visible_mask",
-                        lambda rows, N, causal: (np.arange(N)[None, :] < rows[:, None]) if causal
+                        lambda rows, N, causal, window=0: (np.arange(N)[None, :] < rows[:, None]) if causal
                         else np.ones((len(rows), N), bool))
     with np.errstate(all="ignore"):
         assert not run_pin(pin_causal_row0, ref.attention_forward, ref.attention_backward)
@@ -434,7 +434,7 @@ def test_mutant_strict_causal_is_caught(monkeypatch):
 def test_mutant_off_by_one_causal_is_caught(monkeypatch):
     # Query i also seeing key i + 1.
     monkeypatch.setattr(ref, "visible_mask",
-                        lambda rows, N, causal: (np.arange(N)[None, :] <= rows[:, None] + 1) if causal
+                        lambda rows, N, causal, window=0: (np.arange(N)[None, :] <= rows[:, None] + 1) if causal
                         else np.ones((len(rows), N), bool))
     with np.errstate(all="ignore"):
         assert not run_pin(pin_causal_row0, ref.attention_forward, ref.attention_backward)
@@ -455,3 +455,131 @@ def test_row_range_is_a_partition():
         pb = ref.attention_backward(q, k, v, do, causal, 0.5, row_range=(13, 40))
         for f, a, b in zip(full, pa, pb):
             assert np.allclose(f, a + b, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# Sliding window, decode shapes (Nq < Nk) and the merge of key-split partials.
+# --------------------------------------------------------------------------
+
+def test_window_one_sees_only_itself():
+    # Window 1: query i sees key i alone, so O_i = v_i and LSE_i = s q_i . k_i.
+    q, k, v = (rand((1, 2, 11, 5), s) for s in (200, 201, 202))
+    o, lse = ref.attention_forward(q, k, v, True, 0.3, window=1)
+    assert np.allclose(o, v, atol=1e-13)
+    assert np.allclose(lse, 0.3 * np.einsum("bhnd,bhnd->bhn", q, k), atol=1e-13)
+
+
+def test_window_covering_everything_is_causal():
+    # A window at least as long as the sequence removes nothing.
+    q, k, v, do = (rand((1, 2, 17, 4), s) for s in (210, 211, 212, 213))
+    for w in (17, 40):
+        a = ref.attention_forward(q, k, v, True, 0.5, window=w)
+        b = ref.attention_forward(q, k, v, True, 0.5)
+        assert all(np.allclose(x, y, atol=1e-14) for x, y in zip(a, b))
+        ga = ref.attention_backward(q, k, v, do, True, 0.5, window=w)
+        gb = ref.attention_backward(q, k, v, do, True, 0.5)
+        assert all(np.allclose(x, y, atol=1e-14) for x, y in zip(ga, gb))
+
+
+@pytest.mark.parametrize("w", [2, 3, 6])
+def test_window_matches_brute_force(w):
+    q, k, v, do = (rand((1, 2, 9, 3), s) for s in (220 + w, 221 + w, 222 + w, 223 + w))
+    k1, v1 = k[:, :1], v[:, :1]
+    o, lse = ref.attention_forward(q, k1, v1, True, 0.8, window=w)
+    bo, blse = brute.forward(q.tolist(), k1.tolist(), v1.tolist(), True, 0.8, window=w)
+    assert np.allclose(o, np.array(bo), atol=1e-12) and np.allclose(lse, np.array(blse), atol=1e-12)
+    g = ref.attention_backward(q, k1, v1, do, True, 0.8, window=w)
+    bg = brute.backward(q.tolist(), k1.tolist(), v1.tolist(), do.tolist(), True, 0.8, window=w)
+    assert all(np.allclose(x, np.array(y), atol=1e-12) for x, y in zip(g, bg))
+
+
+def test_window_backward_finite_differences():
+    q, k, v, do = (rand((1, 1, 6, 3), s) for s in (230, 231, 232, 233))
+    w, sc, h = 3, 0.9, 1e-6
+    dq, dk, dv = ref.attention_backward(q, k, v, do, True, sc, window=w)
+
+    def loss(q_, k_, v_):
+        return float(np.sum(do * ref.attention_forward(q_, k_, v_, True, sc, window=w)[0]))
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            argm = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            num[idx] = (loss(*args) - loss(*argm)) / (2 * h)
+        assert np.allclose(num, g, rtol=1e-6, atol=1e-8), name
+
+
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 5)])
+def test_decode_rows_are_the_last_rows(causal, window):
+    # Nq < Nk: the queries are the last Nq positions, so their outputs are the
+    # last Nq rows of self-attention over the full sequence whose last rows
+    # are those queries.
+    Nk, Nq = 23, 4
+    qf = rand((2, 4, Nk, 6), 240)
+    k, v = rand((2, 2, Nk, 6), 241), rand((2, 2, Nk, 6), 242)
+    of, lf = ref.attention_forward(qf, k, v, causal, 0.4, window=window)
+    od, ld = ref.attention_forward(qf[:, :, Nk - Nq:], k, v, causal, 0.4, window=window)
+    assert np.allclose(od, of[:, :, Nk - Nq:], atol=1e-14) and np.allclose(ld, lf[:, :, Nk - Nq:], atol=1e-14)
+
+
+def test_decode_matches_brute_force():
+    q, k, v = rand((1, 2, 3, 4), 250), rand((1, 1, 8, 4), 251), rand((1, 1, 8, 4), 252)
+    for causal, w in ((False, 0), (True, 0), (True, 2)):
+        o, lse = ref.attention_forward(q, k, v, causal, 0.6, window=w)
+        bo, blse = brute.forward(q.tolist(), k.tolist(), v.tolist(), causal, 0.6, window=w)
+        assert np.allclose(o, np.array(bo), atol=1e-12) and np.allclose(lse, np.array(blse), atol=1e-12)
+
+
+def test_causal_needs_enough_keys():
+    with pytest.raises(ValueError):
+        ref.attention_forward(rand((1, 1, 5, 2), 1), rand((1, 1, 3, 2), 2), rand((1, 1, 3, 2), 3), True, 1.0)
+    with pytest.raises(ValueError):
+        ref.attention_forward(rand((1, 1, 5, 2), 1), rand((1, 1, 5, 2), 2), rand((1, 1, 5, 2), 3), False, 1.0,
+                              window=2)
+
+
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 7)])
+def test_merge_of_key_splits_is_exact(causal, window):
+    # Attention over disjoint key chunks, merged, equals attention over all
+    # keys: each chunk's (O, LSE) is the oracle restricted to those keys (the
+    # others masked out), with LSE = -inf where a row sees no key of the chunk.
+    B, Hq, Hkv, N, d, sc = 1, 2, 1, 21, 4, 0.7
+    q, k, v = rand((B, Hq, N, d), 260), rand((B, Hkv, N, d), 261), rand((B, Hkv, N, d), 262)
+    full_o, full_l = ref.attention_forward(q, k, v, causal, sc, window=window)
+    cuts = [0, 5, 6, 14, 21]
+    pos = np.arange(N)
+    parts_o, parts_l = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        s = sc * np.einsum("bhid,bjd->bhij", q, k[:, 0])
+        vis = ref.visible_mask(pos, N, causal, window)
+        vis &= (np.arange(N)[None, :] >= a) & (np.arange(N)[None, :] < b)
+        s = np.where(vis[None, None], s, -np.inf)
+        m = np.max(s, axis=-1, keepdims=True)
+        mf = np.where(np.isfinite(m), m, 0.0)
+        e = np.exp(s - mf)
+        den = e.sum(-1)
+        with np.errstate(all="ignore"):
+            o = np.where(den[..., None] > 0, (e @ v[:, 0][:, None]) / den[..., None], 0.0)
+            l = np.where(den > 0, mf[..., 0] + np.log(den), -np.inf)
+        parts_o.append(o)
+        parts_l.append(l)
+    mo, ml = ref.merge_partials(np.stack(parts_o), np.stack(parts_l))
+    assert np.allclose(mo, full_o, atol=1e-13) and np.allclose(ml, full_l, atol=1e-13)
+
+
+def test_mutant_window_off_by_one_is_caught(monkeypatch):
+    # Window w letting w + 1 keys through.
+    real = ref.visible_mask
+    monkeypatch.setattr(ref, "visible_mask", lambda pos, N, causal, window=0: real(pos, N, causal, window + 1 if window else 0))
+    with pytest.raises(AssertionError):
+        test_window_one_sees_only_itself()
+
+
+def test_mutant_top_left_decode_alignment_is_caught(monkeypatch):
+    # Decode queries placed at the first Nq positions instead of the last.
+    monkeypatch.setattr(ref, "query_positions", lambda rows, Nq, Nk: np.asarray(rows))
+    with pytest.raises(AssertionError):
+        test_decode_rows_are_the_last_rows(True, 0)
