@@ -1,7 +1,8 @@
 """Thin Python binding of libfa_gb300.so (exact IO-aware attention on GB300).
 
-The names ``fa_fwd``, ``fa_bwd``, ``fa_bwd_preprocess``, ``fa_bwd_dkdv``,
-``fa_bwd_dq_convert``, ``fa_bwd_workspace_bytes``, ``fa_strerror``,
+The names ``fa_fwd``, ``fa_fwd_ex``, ``fa_fwd_ex_workspace_bytes``,
+``fa_fwd_ex_default_splits``, ``fa_bwd``, ``fa_bwd_ex``, ``fa_bwd_preprocess``,
+``fa_bwd_dkdv``, ``fa_bwd_dq_convert``, ``fa_bwd_workspace_bytes``, ``fa_strerror``,
 ``fa_last_device_status``, ``fa_selftest_wait_timeout`` and ``fa_version`` are
 the C entry points of ``include/fa.h`` with the same arguments (pointers as
 Python ints, stream as an int handle); they return the integer status.
@@ -56,6 +57,10 @@ _sz = ctypes.c_size_t
 
 _SIGNATURES = {
     "fa_fwd": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p], _i),
+    "fa_fwd_ex": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p, _sz, _p], _i),
+    "fa_fwd_ex_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
+    "fa_fwd_ex_default_splits": ([_i, _i, _i, _i, _i, _i, _i, _i], _i),
+    "fa_bwd_ex": ([_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _sz, _p], _i),
     "fa_bwd_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
     "fa_bwd": ([_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p, _sz, _p], _i),
     "fa_bwd_preprocess": ([_p, _p, _p, _i, _i, _i, _i, _i, _p, _sz, _p], _i),
@@ -107,6 +112,26 @@ def _strerror_safe(status: int) -> str:
 
 def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, stream):
     return load_library().fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, int(causal), float(scale), stream)
+
+
+def fa_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, window, num_splits, scale, workspace,
+              workspace_bytes, stream):
+    return load_library().fa_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, int(causal), int(window),
+                                     int(num_splits), float(scale), workspace, workspace_bytes, stream)
+
+
+def fa_fwd_ex_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, num_splits):
+    return load_library().fa_fwd_ex_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, num_splits)
+
+
+def fa_fwd_ex_default_splits(B, Hq, Hkv, Nq, Nk, d, causal, window):
+    return load_library().fa_fwd_ex_default_splits(B, Hq, Hkv, Nq, Nk, d, int(causal), int(window))
+
+
+def fa_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, window, scale, workspace,
+              workspace_bytes, stream):
+    return load_library().fa_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, int(causal), int(window),
+                                    float(scale), workspace, workspace_bytes, stream)
 
 
 def fa_bwd_workspace_bytes(B, Hq, Hkv, N, d):
@@ -213,6 +238,37 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     return out, lse
 
 
+def forward_ex(q, k, v, causal: bool = False, scale: float | None = None, window: int = 0, num_splits: int = 1,
+               out=None, lse=None, workspace=None, stream=None):
+    """O, LSE of bf16 q [B,Hq,Nq,d] against k, v [B,Hkv,Nk,d] (queries at the last
+    Nq positions), with an optional sliding window and key splits; see fa_fwd_ex.
+    ``num_splits=0`` takes fa_fwd_ex_default_splits."""
+    import torch
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    _check(q, "q", (B, Hq, Nq, d), torch.bfloat16)
+    _check(k, "k", (B, Hkv, Nk, d), torch.bfloat16)
+    _check(v, "v", (B, Hkv, Nk, d), torch.bfloat16)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if num_splits == 0:
+        num_splits = fa_fwd_ex_default_splits(B, Hq, Hkv, Nq, Nk, d, causal, window)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    _check(out, "out", (B, Hq, Nq, d), torch.bfloat16)
+    _check(lse, "lse", (B, Hq, Nq), torch.float32)
+    nbytes = fa_fwd_ex_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, num_splits)
+    if workspace is None and nbytes > 0:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() if workspace is not None else 0
+    _raise(fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Nq, Nk,
+                     d, causal, window, num_splits, scale, wp, wn, _stream_handle(stream)), "fa_fwd_ex")
+    return out, lse
+
+
 def workspace_for(B, Hq, Hkv, N, d, device):
     import torch
     nbytes = fa_bwd_workspace_bytes(B, Hq, Hkv, N, d)
@@ -222,7 +278,7 @@ def workspace_for(B, Hq, Hkv, N, d, device):
 
 
 def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, workspace=None,
-             dq=None, dk=None, dv=None, stream=None):
+             dq=None, dk=None, dv=None, stream=None, window: int = 0):
     """dQ, dK, dV of sum(dO * O), recomputing P from the forward's LSE."""
     import torch
     B, Hq, N, d = q.shape
@@ -237,9 +293,9 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    _raise(fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, causal, scale,
-                  workspace.data_ptr(), workspace.numel(), _stream_handle(stream)), "fa_bwd")
+    _raise(fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, causal, window, scale,
+                     workspace.data_ptr(), workspace.numel(), _stream_handle(stream)), "fa_bwd_ex")
     return dq, dk, dv
 
 

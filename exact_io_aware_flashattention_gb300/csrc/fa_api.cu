@@ -5,6 +5,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -146,6 +147,43 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t elems(int B, int H, int N, int d) { return (size_t)B * H * N * d; }
 
+fa_status check_shape_ex(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+  FA_TRY(check_shape(B, Hq, Hkv, Nq, d));
+  return check_shape(B, Hq, Hkv, Nk, d);
+}
+
+// How the forward tiles a problem: per-head 128-row query tiles, or, for few
+// query rows (Nq < 128, Hq/Hkv * Nq <= 128, Hq > Hkv), one tile holding the
+// rows of all query heads of a kv group; the key tiles split into chunks.
+struct FwdGeometry {
+  int packed, nqt, units, splits, split_tiles;
+};
+FwdGeometry fwd_geometry(int B, int Hq, int Hkv, int Nq, int Nk, int num_splits) {
+  FwdGeometry g;
+  const int G = Hq / Hkv;
+  g.packed = (G > 1 && Nq < 128 && G * Nq <= 128) ? 1 : 0;
+  g.nqt = g.packed ? 1 : (Nq + 127) / 128;
+  g.units = g.packed ? B * Hkv : B * Hq;
+  const int ntk = (Nk + 127) / 128;
+  g.split_tiles = (ntk + num_splits - 1) / num_splits;
+  g.splits = (ntk + g.split_tiles - 1) / g.split_tiles;
+  return g;
+}
+
+// Split forward workspace: per-split O, fp32 [S, B*Hq*Nq, d], then per-split
+// LSE, fp32 [S, B*Hq*Nq], each 256-byte aligned.
+struct FwdWsLayout {
+  size_t o_off, lse_off, total;
+};
+FwdWsLayout fwd_ws_layout(int B, int Hq, int Nq, int d, int num_splits) {
+  const size_t rows = (size_t)B * Hq * Nq;
+  FwdWsLayout w;
+  w.o_off = 0;
+  w.lse_off = align256((size_t)num_splits * rows * d * 4);
+  w.total = w.lse_off + align256((size_t)num_splits * rows * 4);
+  return w;
+}
+
 // Backward workspace: fp32 dQ accumulator [B,Hq,N,d], then LSE*log2(e) and
 // D = rowsum(dO*O), each fp32 [B*Hq, ntp] with ntp = ceil(N/128)*128.
 struct WsLayout {
@@ -167,6 +205,19 @@ fa_status tmap_bf16(CUtensorMap* m, const void* base, int B, int H, int N, int d
   cuuint32_t box[4] = {64, 128, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_LAUNCH;
+}
+
+// Q (or O) [B, Hq, Nq, d] viewed as {d, Hq*Nq, B}: a 128-row box may start at
+// any row of a batch (a tile of one head, or the rows of a group of heads).
+fa_status tmap_rows_bf16(CUtensorMap* m, const void* base, int B, int H, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H * N, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * N * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_LAUNCH;
@@ -208,6 +259,38 @@ fa_status validate_dkdv(const void* q, const void* k, const void* v, const void*
   return FA_OK;
 }
 
+fa_status dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B, int Hq, int Hkv,
+               int N, int d, int causal, int window, float scale, void* workspace, size_t workspace_bytes,
+               void* stream) {
+  FA_TRY(validate_dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
+  DeviceState* ds = nullptr;
+  FA_TRY(device_state(&ds));
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  const WsLayout w = ws_layout(B, Hq, N, d);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  FA_TRY(tmap_bf16(&tq, q, B, Hq, N, d));
+  FA_TRY(tmap_bf16(&tk, k, B, Hkv, N, d));
+  FA_TRY(tmap_bf16(&tv, v, B, Hkv, N, d));
+  FA_TRY(tmap_bf16(&tdo, dO, B, Hq, N, d));
+  FA_TRY(tmap_dq_accum(&tdq, ws + w.dq_off, B, Hq, N, d));
+  fa::BwdArgs a;
+  a.lse2 = reinterpret_cast<const float*>(ws + w.lse2_off);
+  a.drow = reinterpret_cast<const float*>(ws + w.dr_off);
+  a.dq_accum = reinterpret_cast<float*>(ws + w.dq_off);
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.N = N;
+  a.causal = causal;
+  a.window = window;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  return launch_status(
+      fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, tdq, a, dev_status(ds), static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -245,34 +328,86 @@ size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
                  int d, int causal, float scale, void* stream) {
+  return fa_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, N, d, causal, 0, 1, scale, nullptr, 0, stream);
+}
+
+size_t fa_fwd_ex_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_splits) {
+  if (check_shape_ex(B, Hq, Hkv, Nq, Nk, d) != FA_OK || num_splits < 1) return 0;
+  if (num_splits == 1) return 0;
+  return fwd_ws_layout(B, Hq, Nq, d, num_splits).total;
+}
+
+int fa_fwd_ex_default_splits(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window) {
+  if (check_shape_ex(B, Hq, Hkv, Nq, Nk, d) != FA_OK) return 1;
+  DeviceState* ds = nullptr;
+  if (device_state(&ds) != FA_OK) return 1;
+  const FwdGeometry g = fwd_geometry(B, Hq, Hkv, Nq, Nk, 1);
+  // Enough work items for about one per SM; each split keeps >= 4 key tiles.
+  long long units = (long long)g.units * g.nqt;
+  int s = (int)((ds->num_sms + units - 1) / units);
+  int ntk = (Nk + 127) / 128;
+  if (causal && window > 0) ntk = std::min(ntk, (window + 127) / 128 + 1);
+  s = std::min(s, std::max(1, ntk / 4));
+  return std::max(1, std::min(s, 64));
+}
+
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                    int Nk, int d, int causal, int window, int num_splits, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_PTR;
-  FA_TRY(check_shape(B, Hq, Hkv, N, d));
+  FA_TRY(check_shape_ex(B, Hq, Hkv, Nq, Nk, d));
   FA_TRY(check_scale(causal, scale));
+  if (window < 0 || (window > 0 && !causal) || (causal && Nq > Nk) || num_splits < 1 || num_splits > 4096)
+    return FA_ERR_BAD_ARGUMENT;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
-  const size_t qb = elems(B, Hq, N, d) * 2, kb = elems(B, Hkv, N, d) * 2;
+  const FwdGeometry g = fwd_geometry(B, Hq, Hkv, Nq, Nk, num_splits);
+  if ((long long)g.nqt * g.splits * g.units >= (1LL << 31)) return FA_ERR_BAD_SHAPE;
+  const size_t qb = elems(B, Hq, Nq, d) * 2, kb = elems(B, Hkv, Nk, d) * 2;
   const Range ins[] = {range(q, qb), range(k, kb), range(v, kb)};
-  const Range ro = range(o, qb), rl = range(lse, (size_t)B * Hq * N * 4);
+  const Range ro = range(o, qb), rl = range(lse, (size_t)B * Hq * Nq * 4);
   for (const Range& i : ins)
     if (overlap(ro, i) || overlap(rl, i)) return FA_ERR_ALIASING;
   if (overlap(ro, rl)) return FA_ERR_ALIASING;
+  FwdWsLayout w{};
+  if (g.splits > 1) {
+    w = fwd_ws_layout(B, Hq, Nq, d, num_splits);
+    if (!workspace) return FA_ERR_NULL_PTR;
+    if (!aligned16(workspace)) return FA_ERR_MISALIGNED;
+    if (workspace_bytes < w.total) return FA_ERR_WORKSPACE_TOO_SMALL;
+    const Range rw = range(workspace, w.total);
+    for (const Range& i : ins)
+      if (overlap(rw, i)) return FA_ERR_ALIASING;
+    if (overlap(rw, ro) || overlap(rw, rl)) return FA_ERR_ALIASING;
+  }
 
   DeviceState* ds = nullptr;
   FA_TRY(device_state(&ds));
   CUtensorMap tq, tk, tv;
-  FA_TRY(tmap_bf16(&tq, q, B, Hq, N, d));
-  FA_TRY(tmap_bf16(&tk, k, B, Hkv, N, d));
-  FA_TRY(tmap_bf16(&tv, v, B, Hkv, N, d));
+  FA_TRY(tmap_rows_bf16(&tq, q, B, Hq, Nq, d));
+  FA_TRY(tmap_bf16(&tk, k, B, Hkv, Nk, d));
+  FA_TRY(tmap_bf16(&tv, v, B, Hkv, Nk, d));
   fa::FwdArgs a;
   a.o = o;
   a.lse = lse;
+  a.o_part = g.splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.o_off) : nullptr;
+  a.lse_part = g.splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.lse_off) : nullptr;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
-  a.N = N;
+  a.Nq = Nq;
+  a.Nk = Nk;
   a.causal = causal;
+  a.window = window;
+  a.packed = g.packed;
+  a.nqt = g.nqt;
+  a.units = g.units;
+  a.splits = g.splits;
+  a.split_tiles = g.split_tiles;
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_status(
-      fa::launch_fwd(d, tq, tk, tv, a, dev_status(ds), ds->num_sms, static_cast<cudaStream_t>(stream)));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  FA_TRY(launch_status(fa::launch_fwd(d, tq, tk, tv, a, dev_status(ds), ds->num_sms, st)));
+  if (g.splits > 1) FA_TRY(launch_status(fa::launch_fwd_merge(d, a, ds->num_sms, st)));
+  return FA_OK;
 }
 
 fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, int B, int Hq, int Hkv, int N, int d,
@@ -297,33 +432,10 @@ fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, int
 fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B, int Hq,
                       int Hkv, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
                       void* stream) {
-  FA_TRY(validate_dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
-  DeviceState* ds = nullptr;
-  FA_TRY(device_state(&ds));
-  CUtensorMap tq, tk, tv, tdo, tdq;
-  const WsLayout w = ws_layout(B, Hq, N, d);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  FA_TRY(tmap_bf16(&tq, q, B, Hq, N, d));
-  FA_TRY(tmap_bf16(&tk, k, B, Hkv, N, d));
-  FA_TRY(tmap_bf16(&tv, v, B, Hkv, N, d));
-  FA_TRY(tmap_bf16(&tdo, dO, B, Hq, N, d));
-  FA_TRY(tmap_dq_accum(&tdq, ws + w.dq_off, B, Hq, N, d));
-  fa::BwdArgs a;
-  a.lse2 = reinterpret_cast<const float*>(ws + w.lse2_off);
-  a.drow = reinterpret_cast<const float*>(ws + w.dr_off);
-  a.dq_accum = reinterpret_cast<float*>(ws + w.dq_off);
-  a.dk = dk;
-  a.dv = dv;
-  a.B = B;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.N = N;
-  a.causal = causal;
-  a.scale = scale;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_status(
-      fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, tdq, a, dev_status(ds), static_cast<cudaStream_t>(stream)));
+  return dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, 0, scale, workspace, workspace_bytes, stream);
 }
+
+
 
 fa_status fa_bwd_dq_convert(void* dq, int B, int Hq, int Hkv, int N, int d, float scale, const void* workspace,
                             size_t workspace_bytes, void* stream) {
@@ -345,7 +457,15 @@ fa_status fa_bwd_dq_convert(void* dq, int B, int Hq, int Hkv, int N, int d, floa
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                  void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                  void* workspace, size_t workspace_bytes, void* stream) {
+  return fa_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, 0, scale, workspace, workspace_bytes,
+                   stream);
+}
+
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                    void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                    float scale, void* workspace, size_t workspace_bytes, void* stream) {
   if (!o || !dq || !lse) return FA_ERR_NULL_PTR;
+  if (window < 0 || (window > 0 && !causal)) return FA_ERR_BAD_ARGUMENT;
   FA_TRY(validate_dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
   if (!aligned16(o) || !aligned16(dq) || !aligned16(lse)) return FA_ERR_MISALIGNED;
   const size_t qb = elems(B, Hq, N, d) * 2, kb = elems(B, Hkv, N, d) * 2;
@@ -360,7 +480,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (overlap(ro, range(dk, kb)) || overlap(ro, range(dv, kb)) || overlap(ro, rw)) return FA_ERR_ALIASING;
   if (overlap(rl, range(dk, kb)) || overlap(rl, range(dv, kb)) || overlap(rl, rw)) return FA_ERR_ALIASING;
   FA_TRY(fa_bwd_preprocess(o, dO, lse, B, Hq, Hkv, N, d, workspace, workspace_bytes, stream));
-  FA_TRY(fa_bwd_dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes, stream));
+  FA_TRY(dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, window, scale, workspace, workspace_bytes, stream));
   return fa_bwd_dq_convert(dq, B, Hq, Hkv, N, d, scale, workspace, workspace_bytes, stream);
 }
 

@@ -113,7 +113,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nt = (N + kT - 1) / kT;
   const int G = args.Hq / args.Hkv;
   const int i0 = args.causal ? j : 0;            // first query tile that sees key tile j
-  const int nqi = nt - i0;
+  // One past the last query tile that sees key tile j: with a window w the
+  // last query to see key 128j + 127 is 128j + 126 + w.
+  const int i1 = args.window > 0 ? min(nt, (j * kT + kT - 2 + args.window) / kT + 1) : nt;
+  const int nqi = i1 - i0;
   const int n_items = G * nqi;
 
   if (threadIdx.x == 0) {
@@ -312,9 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P^T[key, q] = 2^(s * sl2 - lse2[q]); zero where the key is past N or
       // (diagonal tile, causal) after the query.  Query rows past N have
       // lse2 = +inf in the padded array, which gives 0.
-      int lim = 64;                                // visible query columns are [c0 + 64 - lim, c0 + 64)
-      if (key >= N) lim = 0;
-      else if (args.causal && i == j) lim = min(64, max(0, c0 + 64 - r));
+      // This key is visible to the group's query columns [clo, chi): causal
+      // needs query >= key, a window w also query < key + w.
+      const int qcol0 = i * kT + c0;               // query index of the group's column 0
+      int clo = args.causal ? min(64, max(0, key - qcol0)) : 0;
+      const int chi = args.window > 0 ? min(64, max(0, key + args.window - qcol0)) : 64;
+      if (key >= N) clo = 64;
       uint32_t pk[32];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -328,8 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2unpack(ffma2(f2pack(__uint_as_float(pr[q][e]), __uint_as_float(pr[q][e + 1])), sl2x2,
                          f2pack(-la, -lb)),
                    lo, hi);
-          lo = (col >= 64 - lim) ? ex2(lo) : 0.f;
-          hi = (col + 1 >= 64 - lim) ? ex2(hi) : 0.f;
+          lo = (col >= clo && col < chi) ? ex2(lo) : 0.f;
+          hi = (col + 1 >= clo && col + 1 < chi) ? ex2(hi) : 0.f;
           pr[q][e] = __float_as_uint(lo);
           pr[q][e + 1] = __float_as_uint(hi);
           pk[col >> 1] = cvt_bf16x2(lo, hi);

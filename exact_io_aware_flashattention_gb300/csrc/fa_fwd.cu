@@ -89,21 +89,60 @@ struct Bars {
 };
 
 struct Item {
-  int qt, h, b, kvh, n;
+  int b, h, kvh;     // batch, first query head of the tile, kv head
+  int qrow;          // Q map row (within batch b) of tile row 0: h * Nq + first query index
+  long long row0;    // flattened [B*Hq*Nq] row of tile row 0
+  int rows;          // tile rows that are real query rows
+  int qbase;         // query index of tile row 0 (per-head tiles), 0 when packed
+  int qmin, qmax;    // smallest / largest query position in the tile
+  int j0, n;         // key tiles [j0, j0 + n)
+  int split;
 };
 
-// Work items are ordered heaviest first: rank r covers query tile nt-1-r of
-// every (head, batch) when causal (tile r otherwise).
-__device__ __forceinline__ Item decode_item(int idx, const FwdArgs& a, int nt) {
-  const int per = a.Hq * a.B;
-  const int rank = idx / per;
-  const int hb = idx - rank * per;
+// A query tile is 128 consecutive query rows of one head, or, when packed,
+// the rows of all Hq/Hkv heads of one kv group (G * Nq <= 128 rows), so that
+// the group reads each K / V tile once.  Query row i stands at key position
+// i + Nk - Nq.  Work items are ordered heaviest first: rank r covers query
+// tile nqt-1-r of every unit when causal (tile r otherwise), each split of it
+// in turn.  An item may own no key tile (a split outside the tile's visible
+// range); every role skips such items.
+__device__ __forceinline__ Item decode_item(int idx, const FwdArgs& a) {
+  const int rs = idx / a.units;
+  const int u = idx - rs * a.units;
+  const int rank = rs / a.splits;
   Item it;
-  it.qt = a.causal ? nt - 1 - rank : rank;
-  it.h = hb % a.Hq;
-  it.b = hb / a.Hq;
-  it.kvh = it.h / (a.Hq / a.Hkv);
-  it.n = a.causal ? min(it.qt + 1, nt) : nt;
+  it.split = rs - rank * a.splits;
+  const int qt = a.causal ? a.nqt - 1 - rank : rank;
+  const int G = a.Hq / a.Hkv;
+  const int off = a.Nk - a.Nq;
+  if (a.packed) {
+    it.kvh = u % a.Hkv;
+    it.b = u / a.Hkv;
+    it.h = it.kvh * G;
+    it.qbase = 0;
+    it.rows = G * a.Nq;
+    it.qmin = off;
+    it.qmax = a.Nq - 1 + off;
+  } else {
+    it.h = u % a.Hq;
+    it.b = u / a.Hq;
+    it.kvh = it.h / G;
+    it.qbase = qt * kBM;
+    it.rows = min(kBM, a.Nq - it.qbase);
+    it.qmin = it.qbase + off;
+    it.qmax = it.qbase + it.rows - 1 + off;
+  }
+  it.qrow = it.h * a.Nq + it.qbase;
+  it.row0 = (long long)it.b * a.Hq * a.Nq + it.qrow;
+  const int ntk = (a.Nk + kBN - 1) / kBN;
+  int hi = a.causal ? min(ntk, it.qmax / kBN + 1) : ntk;
+  int lo = a.window > 0 ? max(0, it.qmin - a.window + 1) / kBN : 0;
+  if (a.splits > 1) {
+    lo = max(lo, it.split * a.split_tiles);
+    hi = min(hi, (it.split + 1) * a.split_tiles);
+  }
+  it.j0 = lo;
+  it.n = max(0, hi - lo);
   return it;
 }
 
@@ -115,27 +154,35 @@ __device__ __forceinline__ int item_of_round(int k) {
   return k * g + ((k & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x);
 }
 
-// Walks this CTA's (item, key tile) sequence.
+// Walks this CTA's (item, key tile) sequence over the items that own key
+// tiles; li counts those items.
 struct Cursor {
-  int item, li, j, n_items, nt;
+  int item, round, li, j, n_items;
   Item it;
   bool valid;
-  __device__ __forceinline__ void init(const FwdArgs& a, int nt_, int n_items_) {
-    nt = nt_;
+  __device__ __forceinline__ void seek(const FwdArgs& a) {
+    for (;;) {
+      item = item_of_round(round);
+      valid = item < n_items;
+      if (!valid) return;
+      it = decode_item(item, a);
+      if (it.n > 0) return;
+      ++round;
+    }
+  }
+  __device__ __forceinline__ void init(const FwdArgs& a, int n_items_) {
     n_items = n_items_;
+    round = 0;
     li = 0;
     j = 0;
-    item = item_of_round(0);
-    valid = item < n_items;
-    if (valid) it = decode_item(item, a, nt);
+    seek(a);
   }
   __device__ __forceinline__ void next(const FwdArgs& a) {
     if (++j == it.n) {
       j = 0;
       ++li;
-      item = item_of_round(li);
-      valid = item < n_items;
-      if (valid) it = decode_item(item, a, nt);
+      ++round;
+      seek(a);
     }
   }
 };
@@ -160,9 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int N = args.N;
-  const int nt = (N + kBM - 1) / kBM;
-  const int n_items = nt * args.Hq * args.B;
+  const int Nk = args.Nk;
+  const int n_items = args.nqt * args.splits * args.units;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -215,23 +261,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kt = 0, li = 0;
       int q_issued[2] = {0, 0};
       bool ok = true;
-      for (int item = item_of_round(0); ok && item < n_items; item = item_of_round(++li)) {
-        const Item it = decode_item(item, args, nt);
+      for (int round = 0, item = item_of_round(0); ok && item < n_items; item = item_of_round(++round)) {
+        const Item it = decode_item(item, args);
+        if (it.n == 0) continue;
         const int slot = li & 1;
         if (li >= 2 && !mbar_wait(&bars->q_empty[slot], ((li >> 1) - 1) & 1, st, abort_flag, kSiteQEmpty)) break;
         mbar_arrive_expect_tx(&bars->q_full[slot], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
-          tma_load_4d(smem + L::kQ + slot * L::kTile + a * kBlockBytes, &tmQ, &bars->q_full[slot], a * 64,
-                      it.qt * kBM, it.h, it.b);
+          tma_load_3d(smem + L::kQ + slot * L::kTile + a * kBlockBytes, &tmQ, &bars->q_full[slot], a * 64,
+                      it.qrow, it.b);
         ++q_issued[slot];
         for (int j = 0; j < it.n; ++j, ++kt) {
           const int s = kt % SK, r = kt / SK;
           if (r > 0 && !mbar_wait(&bars->k_empty[s], (r - 1) & 1, st, abort_flag, kSiteKEmpty)) { ok = false; break; }
           mbar_arrive_expect_tx(&bars->k_full[s], L::kTile);
           for (int a = 0; a < kAtoms; ++a)
-            tma_load_4d(smem + L::kK + s * L::kTile + a * kBlockBytes, &tmK, &bars->k_full[s], a * 64, j * kBN,
-                        it.kvh, it.b);
+            tma_load_4d(smem + L::kK + s * L::kTile + a * kBlockBytes, &tmK, &bars->k_full[s], a * 64,
+                        (it.j0 + j) * kBN, it.kvh, it.b);
         }
+        ++li;   // items with key tiles, in the order the MMA issuers' cursors count them
       }
       // Every copy issued must have landed before the CTA may exit.
       for (int i = 0; i < 2; ++i)
@@ -247,14 +295,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int vt = 0;
       bool ok = true;
       for (int round = 0, item = item_of_round(0); ok && item < n_items; item = item_of_round(++round)) {
-        const Item it = decode_item(item, args, nt);
+        const Item it = decode_item(item, args);
         for (int j = 0; j < it.n; ++j, ++vt) {
           const int s = vt % SV, r = vt / SV;
           if (r > 0 && !mbar_wait(&bars->v_empty[s], (r - 1) & 1, st, abort_flag, kSiteVEmpty)) { ok = false; break; }
           mbar_arrive_expect_tx(&bars->v_full[s], L::kTile);
           for (int a = 0; a < kAtoms; ++a)
-            tma_load_4d(smem + L::kV + s * L::kTile + a * kBlockBytes, &tmV, &bars->v_full[s], a * 64, j * kBN,
-                        it.kvh, it.b);
+            tma_load_4d(smem + L::kV + s * L::kTile + a * kBlockBytes, &tmV, &bars->v_full[s], a * 64,
+                        (it.j0 + j) * kBN, it.kvh, it.b);
         }
       }
       for (int s = 0; s < SV && s < vt; ++s) {
@@ -267,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
       Cursor sc;
-      sc.init(args, nt, n_items);
+      sc.init(args, n_items);
       for (int ts = 0; sc.valid; ++ts, sc.next(args)) {
         const int buf = ts % kSBuf;
         // S_ts reuses score buffer ts % 2 once the owner of tile ts-2 has read it.
@@ -297,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
       Cursor pc;
-      pc.init(args, nt, n_items);
+      pc.init(args, n_items);
       for (int t = 0; pc.valid; ++t, pc.next(args)) {
         const int buf = t % kSBuf;
         if (!mbar_wait(&bars->p_full[buf], (t / kSBuf) & 1, st, abort_flag, kSitePFull)) break;
@@ -331,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int my_item = -1;                            // item the group's (l_g, m_g) belong to
     int n_multi = 0;                             // items with >= 2 tiles completed so far
     Cursor c;
-    c.init(args, nt, n_items);
+    c.init(args, n_items);
     for (int t = 0; c.valid; ++t, c.next(args)) {
       const int j = c.j, n = c.it.n;
       const int n_multi_before = n_multi;
@@ -339,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j == n - 1 && n >= 2) ++n_multi;
       if ((t & 1) != g) continue;                // the other group's tile
       const int buf = t % kSBuf;
-      const int row = c.it.qt * kBM + r;
+      // Position of this thread's query among the keys.
+      const int qpos = (args.packed ? r % args.Nq : c.it.qbase + r) + (Nk - args.Nq);
       const uint32_t tS = tmem + buf * 128 + lane_off;
       if (!mbar_wait_warp(&bars->s_full[buf], (t / kSBuf) & 1, st, abort_flag, kSiteSFull)) break;
       tc_fence_after();
@@ -352,14 +401,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->s_free[buf]);   // the MMA may compute S_{t+2} into this buffer now
 
-      const int key0 = j * kBN;
-      if ((key0 + kBN > N) || (args.causal && j == c.it.qt)) {
-        const int lim = min(N, args.causal ? row + 1 : N) - key0;   // keys [key0, key0 + lim) are visible
+      const int key0 = (c.it.j0 + j) * kBN;
+      if ((key0 + kBN > Nk) || (args.causal && key0 + kBN - 1 > c.it.qmin) ||
+          (args.window > 0 && key0 < c.it.qmax - args.window + 1)) {
+        // Keys [key0 + lo, key0 + hi) are visible to this row.
+        const int hi = min(Nk, args.causal ? qpos + 1 : Nk) - key0;
+        const int lo = args.window > 0 ? qpos - args.window + 1 - key0 : 0;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (q * 32 + e >= lim) sr[q][e] = __float_as_uint(-INFINITY);
+            if (q * 32 + e >= hi || q * 32 + e < lo) sr[q][e] = __float_as_uint(-INFINITY);
       }
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -481,23 +533,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < D / 32; ++q) reg_fence(o[q]);
         tc_fence_before();
         mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
-        const float inv_l = 1.f / l_tot;
-        const size_t head = (size_t)c.it.b * args.Hq + c.it.h;
-        if (row < N) {
-          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.o) + (head * N + (size_t)row) * D;
+        const long long frow = c.it.row0 + r;
+        if (r < c.it.rows) {
+          if (args.splits == 1) {
+            const float inv_l = 1.f / l_tot;
+            __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.o) + frow * D;
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
+            for (int q = 0; q < D / 32; ++q) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 0]) * inv_l, __uint_as_float(o[q][v * 8 + 1]) * inv_l);
-              w.y = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 2]) * inv_l, __uint_as_float(o[q][v * 8 + 3]) * inv_l);
-              w.z = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 4]) * inv_l, __uint_as_float(o[q][v * 8 + 5]) * inv_l);
-              w.w = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 6]) * inv_l, __uint_as_float(o[q][v * 8 + 7]) * inv_l);
-              *reinterpret_cast<uint4*>(orow + q * 32 + v * 8) = w;
+              for (int v = 0; v < 4; ++v) {
+                uint4 w;
+                w.x = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 0]) * inv_l, __uint_as_float(o[q][v * 8 + 1]) * inv_l);
+                w.y = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 2]) * inv_l, __uint_as_float(o[q][v * 8 + 3]) * inv_l);
+                w.z = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 4]) * inv_l, __uint_as_float(o[q][v * 8 + 5]) * inv_l);
+                w.w = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 6]) * inv_l, __uint_as_float(o[q][v * 8 + 7]) * inv_l);
+                *reinterpret_cast<uint4*>(orow + q * 32 + v * 8) = w;
+              }
             }
+            args.lse[frow] = (m_new + __log2f(l_tot)) * 0.69314718055994530942f;
+          } else {
+            // One key split: O normalised within the split, fp32, and its LSE;
+            // a row that sees no key of the split gets O = 0, LSE = -inf.
+            const long long prow = (long long)c.it.split * args.B * args.Hq * args.Nq + frow;
+            const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            float4* orow = reinterpret_cast<float4*>(args.o_part + prow * D);
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q)
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                orow[q * 8 + v] = make_float4(__uint_as_float(o[q][v * 4 + 0]) * inv_l,
+                                              __uint_as_float(o[q][v * 4 + 1]) * inv_l,
+                                              __uint_as_float(o[q][v * 4 + 2]) * inv_l,
+                                              __uint_as_float(o[q][v * 4 + 3]) * inv_l);
+            args.lse_part[prow] =
+                l_tot > 0.f ? (m_new + __log2f(l_tot)) * 0.69314718055994530942f : -INFINITY;
           }
-          args.lse[head * N + row] = (m_new + __log2f(l_tot)) * 0.69314718055994530942f;
         }
       }
     }
@@ -522,8 +592,7 @@ static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, co
   static_assert(sizeof(Bars) <= 512, "barrier block");
   cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
-  const long long nt = (a.N + kBM - 1) / kBM;
-  const long long items = nt * a.Hq * a.B;
+  const long long items = (long long)a.nqt * a.splits * a.units;
   const int grid = (int)(items < num_sms ? items : num_sms);
   fa_fwd_kernel<D><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, a, st);
   return cudaGetLastError();
@@ -533,6 +602,63 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        const DevStatus& st, int num_sms, cudaStream_t stream) {
   if (d == 64) return launch_fwd_d<64>(tq, tk, tv, a, st, num_sms, stream);
   return launch_fwd_d<128>(tq, tk, tv, a, st, num_sms, stream);
+}
+
+// Merge of the key splits ([Lecture] "推导 FlashAttention 的在线 softmax": both
+// parts of a softmax-weighted sum are carried relative to a reference max and
+// rescaled by exp(old - new) when the reference changes).  For query row r
+// with split results (O_s, LSE_s): m = max_s LSE_s, w_s = exp(LSE_s - m),
+// O = sum_s w_s O_s / sum_s w_s, LSE = m + ln sum_s w_s.  Splits that hold no
+// key the row may see were either not computed or hold LSE = -inf; both are
+// skipped.  One thread per 4 columns of a row.
+template <int D>
+__global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const FwdArgs a) {
+  constexpr int kC4 = D / 4;
+  const long long R = (long long)a.B * a.Hq * a.Nq;
+  const long long total = R * kC4;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const long long row = idx / kC4;
+    const int c4 = (int)(idx - row * kC4);
+    const int qpos = (int)(row % a.Nq) + a.Nk - a.Nq;
+    const int klo = a.window > 0 ? max(0, qpos - a.window + 1) : 0;   // visible keys [klo, khi)
+    const int khi = a.causal ? min(a.Nk, qpos + 1) : a.Nk;
+    const int span = a.split_tiles * kBN;
+    const int s0 = klo / span, s1 = (khi - 1) / span;                 // splits holding visible keys
+    float m = -INFINITY;
+    for (int s = s0; s <= s1; ++s) m = fmaxf(m, a.lse_part[s * R + row]);
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = s0; s <= s1; ++s) {
+      const float ls = a.lse_part[s * R + row];
+      if (ls == -INFINITY) continue;
+      const float w = __expf(ls - m);
+      const float4 o = reinterpret_cast<const float4*>(a.o_part + (s * R + row) * D)[c4];
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
+      den += w;
+    }
+    const float inv = 1.f / den;
+    uint2 out;
+    out.x = cvt_bf16x2(acc.x * inv, acc.y * inv);
+    out.y = cvt_bf16x2(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.o) + row * D)[c4] = out;
+    if (c4 == 0) a.lse[row] = m + __logf(den);
+  }
+}
+
+cudaError_t launch_fwd_merge(int d, const FwdArgs& a, int num_sms, cudaStream_t stream) {
+  const long long total = (long long)a.B * a.Hq * a.Nq * (d / 4);
+  long long blocks = (total + 255) / 256;
+  if (blocks > (long long)num_sms * 8) blocks = (long long)num_sms * 8;
+  if (blocks < 1) blocks = 1;
+  if (d == 64)
+    fa_fwd_merge_kernel<64><<<(int)blocks, 256, 0, stream>>>(a);
+  else
+    fa_fwd_merge_kernel<128><<<(int)blocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace fa

@@ -11,10 +11,18 @@
 namespace fa {
 
 struct FwdArgs {
-  void* o;            // [B, Hq, N, d] bf16
-  float* lse;         // [B, Hq, N] fp32, natural log
-  int B, Hq, Hkv, N;
-  int causal;
+  void* o;            // [B, Hq, Nq, d] bf16 (one split)
+  float* lse;         // [B, Hq, Nq] fp32, natural log (one split)
+  float* o_part;      // [splits, B*Hq*Nq, d] fp32 per-split O (several splits, workspace)
+  float* lse_part;    // [splits, B*Hq*Nq] fp32 per-split LSE (several splits, workspace)
+  int B, Hq, Hkv, Nq, Nk;
+  int causal;         // key j visible to query row i iff j <= i + Nk - Nq
+  int window;         // > 0: also j > i + Nk - Nq - window
+  int packed;         // a query tile holds all Hq/Hkv heads of a kv group (Hq/Hkv * Nq <= 128)
+  int nqt;            // query tiles per unit (1 when packed)
+  int units;          // B*Hq, or B*Hkv when packed
+  int splits;         // key range split into chunks of split_tiles 128-key tiles
+  int split_tiles;
   float scale_log2;   // scale * log2(e)
 };
 
@@ -26,12 +34,16 @@ struct BwdArgs {
   void* dv;           // [B, Hkv, N, d] bf16
   int B, Hq, Hkv, N;
   int causal;
+  int window;         // > 0: key j visible to query i only if j > i - window (with causal)
   float scale;        // softmax scale
   float scale_log2;   // scale * log2(e)
 };
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
                        const DevStatus& st, int num_sms, cudaStream_t stream);
+
+// (O, LSE) of several key splits -> O (bf16), LSE.
+cudaError_t launch_fwd_merge(int d, const FwdArgs& a, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dO, const float* lse, float* lse2, float* drow,
                                   float* dq_accum, long long heads, int N, int num_sms, cudaStream_t stream);

@@ -167,6 +167,14 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Tiled 3-D reduce-add of a shared-memory box into global memory (the tensor
 // map's element type and reduction), tracked by this thread's bulk group.
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t ssrc, int c0, int c1, int c2) {

@@ -74,6 +74,51 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int d, int causal, float scale, void* stream);
 
 /*
+ * Generalised forward: fa_fwd with these extensions.
+ *   - Nq query rows against Nk keys (q, o: [B,Hq,Nq,d]; k, v: [B,Hkv,Nk,d];
+ *     lse: [B,Hq,Nq]).  The queries are the last Nq positions: query row i
+ *     stands at key position p_i = i + Nk - Nq (the decode shape: a few new
+ *     queries attending to a long key/value history).  Nq == Nk == N is fa_fwd.
+ *   - causal = 1: key j is visible to query row i iff j <= p_i (needs Nq <= Nk).
+ *   - window = w >= 1 (needs causal = 1): also j > p_i - w, a sliding local
+ *     window, the visibility pattern the pages ("ZeRO 与 FlashAttention 各优化
+ *     什么?", 注意力瓶颈与优化路线; "38.解释FlashAttention的显存优化原理", part 2)
+ *     name as an alternative to full attention.  window = 0: no window.
+ *   - num_splits = S >= 1: the key tiles are cut into S contiguous chunks that
+ *     are computed independently (more parallel work for few query rows); each
+ *     chunk's (O_s, LSE_s) goes to the workspace and a second kernel merges
+ *     them: O = sum_s e^(LSE_s - m) O_s / sum_s e^(LSE_s - m), LSE = m + ln
+ *     sum_s e^(LSE_s - m), m = max_s LSE_s -- the streaming-softmax rescale of
+ *     "推导 FlashAttention 的在线 softmax" applied to whole chunks.  S = 1 needs
+ *     no workspace (workspace may be NULL) and is one kernel launch.
+ * When Hq > Hkv and Nq is small (Hq/Hkv * Nq <= 128, Nq < 128) the query
+ * rows of all heads of a kv group share one 128-row tile, so each K/V tile is
+ * read once per group.
+ * Errors: FA_ERR_BAD_ARGUMENT for window < 0, window > 0 without causal,
+ * causal with Nq > Nk, or num_splits outside [1, 4096];
+ * FA_ERR_WORKSPACE_TOO_SMALL if S > 1 and workspace_bytes <
+ * fa_fwd_ex_workspace_bytes(...); otherwise as fa_fwd.  Outputs must not
+ * overlap inputs, each other or the workspace.
+ */
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                    int Nk, int d, int causal, int window, int num_splits, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes fa_fwd_ex needs for num_splits splits: per-split O, fp32
+ * [S, B*Hq*Nq, d], then per-split LSE, fp32 [S, B*Hq*Nq], each rounded up to
+ * 256 bytes.  0 for num_splits == 1 or invalid shapes.
+ */
+size_t fa_fwd_ex_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_splits);
+
+/*
+ * A split count for fa_fwd_ex on the current device: enough work items for
+ * about one per SM, at least 4 key tiles per split, at most 64 splits.
+ * Returns 1 for problems that already fill the GPU (or invalid shapes).
+ */
+int fa_fwd_ex_default_splits(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window);
+
+/*
  * Bytes of device workspace fa_bwd needs: the fp32 dQ accumulator
  * [B,Hq,N,d], then LSE*log2(e) and the row term D = rowsum(dO * O), each
  * fp32 [B*Hq, ceil(N/128)*128]; every part rounded up to 256 bytes.
@@ -94,6 +139,18 @@ size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                  void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_bwd with a sliding window (see fa_fwd_ex): window = w >= 1 with causal
+ * = 1 recomputes P with key j visible to query i iff i - w < j <= i, and
+ * only visits the (query tile, key tile) pairs inside that band; window = 0
+ * is fa_bwd.  Self-attention only (Nq == Nk == N).  FA_ERR_BAD_ARGUMENT for
+ * window < 0 or window > 0 without causal; otherwise as fa_bwd.  o and lse
+ * must come from the forward with the same window.
+ */
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                    void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                    float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Backward step 1: D = rowsum(dO * O) and LSE * log2(e) into the workspace

@@ -115,3 +115,46 @@ def test_bwd_rejects_bad_arguments(lib):
 
 def test_selftest_rejects_bad_limit(lib):
     assert fa.fa_selftest_wait_timeout(10) == fa.FA_ERR_BAD_ARGUMENT
+
+
+def _fwd_ex(**kw):
+    args = dict(q=A, k=2 * A, v=3 * A, o=4 * A, lse=5 * A, B=1, Hq=2, Hkv=1, Nq=4, Nk=300, d=64, causal=1, window=0,
+                num_splits=1, scale=0.125, workspace=None, workspace_bytes=0, stream=None)
+    args.update(kw)
+    return fa.fa_fwd_ex(**args)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(window=-1), fa.FA_ERR_BAD_ARGUMENT),
+    (dict(window=4, causal=0), fa.FA_ERR_BAD_ARGUMENT),
+    (dict(Nq=400), fa.FA_ERR_BAD_ARGUMENT),          # causal with more queries than keys
+    (dict(num_splits=0), fa.FA_ERR_BAD_ARGUMENT),
+    (dict(Nk=0), fa.FA_ERR_BAD_SHAPE),
+    (dict(num_splits=2), fa.FA_ERR_NULL_PTR),        # splits need a workspace
+    (dict(num_splits=2, workspace=6 * A, workspace_bytes=64), fa.FA_ERR_WORKSPACE_TOO_SMALL),
+    (dict(num_splits=2, workspace=6 * A + 4, workspace_bytes=1 << 20), fa.FA_ERR_MISALIGNED),
+    (dict(num_splits=2, workspace=A, workspace_bytes=1 << 20), fa.FA_ERR_ALIASING),
+])
+def test_fwd_ex_rejects_bad_arguments(lib, kw, status):
+    assert _fwd_ex(**kw) == status
+
+
+def test_fwd_ex_workspace_formula(lib):
+    # Per-split O fp32 [S, B*Hq*Nq, d] then per-split LSE fp32 [S, B*Hq*Nq], 256-B aligned parts.
+    r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for B, Hq, Hkv, Nq, Nk, d, S in [(1, 8, 2, 1, 8192, 128, 8), (4, 32, 8, 3, 32768, 64, 16), (2, 2, 2, 100, 300, 64, 3)]:
+        rows = B * Hq * Nq
+        assert fa.fa_fwd_ex_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, S) == r256(S * rows * d * 4) + r256(S * rows * 4)
+    assert fa.fa_fwd_ex_workspace_bytes(1, 8, 2, 1, 8192, 128, 1) == 0
+    assert fa.fa_fwd_ex_workspace_bytes(1, 8, 3, 1, 8192, 128, 4) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(window=-1), fa.FA_ERR_BAD_ARGUMENT),
+    (dict(window=8, causal=0), fa.FA_ERR_BAD_ARGUMENT),
+])
+def test_bwd_ex_rejects_bad_window(lib, kw, status):
+    args = dict(q=A, k=2 * A, v=3 * A, o=4 * A, do=5 * A, lse=6 * A, dq=7 * A, dk=8 * A, dv=9 * A, B=1, Hq=1, Hkv=1,
+                N=16, d=64, causal=1, window=0, scale=0.125, workspace=10 * A, workspace_bytes=1 << 20, stream=None)
+    args.update(kw)
+    assert fa.fa_bwd_ex(**args) == status
