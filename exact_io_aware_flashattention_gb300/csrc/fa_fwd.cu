@@ -106,16 +106,21 @@ struct Item {
 // tile nqt-1-r of every unit when causal (tile r otherwise), each split of it
 // in turn.  An item may own no key tile (a split outside the tile's visible
 // range); every role skips such items.
+// kGeneral = false compiles the plain self-attention case only (Nq == Nk, no
+// window, one split, per-head tiles), so the common path carries none of the
+// general path's code.
+template <bool kGeneral>
 __device__ __forceinline__ Item decode_item(int idx, const FwdArgs& a) {
+  const int splits = kGeneral ? a.splits : 1;
   const int rs = idx / a.units;
   const int u = idx - rs * a.units;
-  const int rank = rs / a.splits;
+  const int rank = rs / splits;
   Item it;
-  it.split = rs - rank * a.splits;
+  it.split = rs - rank * splits;
   const int qt = a.causal ? a.nqt - 1 - rank : rank;
   const int G = a.Hq / a.Hkv;
-  const int off = a.Nk - a.Nq;
-  if (a.packed) {
+  const int off = kGeneral ? a.Nk - a.Nq : 0;
+  if (kGeneral && a.packed) {
     it.kvh = u % a.Hkv;
     it.b = u / a.Hkv;
     it.h = it.kvh * G;
@@ -136,8 +141,8 @@ __device__ __forceinline__ Item decode_item(int idx, const FwdArgs& a) {
   it.row0 = (long long)it.b * a.Hq * a.Nq + it.qrow;
   const int ntk = (a.Nk + kBN - 1) / kBN;
   int hi = a.causal ? min(ntk, it.qmax / kBN + 1) : ntk;
-  int lo = a.window > 0 ? max(0, it.qmin - a.window + 1) / kBN : 0;
-  if (a.splits > 1) {
+  int lo = (kGeneral && a.window > 0) ? max(0, it.qmin - a.window + 1) / kBN : 0;
+  if (kGeneral && a.splits > 1) {
     lo = max(lo, it.split * a.split_tiles);
     hi = min(hi, (it.split + 1) * a.split_tiles);
   }
@@ -156,6 +161,7 @@ __device__ __forceinline__ int item_of_round(int k) {
 
 // Walks this CTA's (item, key tile) sequence over the items that own key
 // tiles; li counts those items.
+template <bool kGeneral>
 struct Cursor {
   int item, round, li, j, n_items;
   Item it;
@@ -165,7 +171,7 @@ struct Cursor {
       item = item_of_round(round);
       valid = item < n_items;
       if (!valid) return;
-      it = decode_item(item, a);
+      it = decode_item<kGeneral>(item, a);
       if (it.n > 0) return;
       ++round;
     }
@@ -187,7 +193,7 @@ struct Cursor {
   }
 };
 
-template <int D>
+template <int D, bool kGeneral>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args, const DevStatus st) {
@@ -262,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_issued[2] = {0, 0};
       bool ok = true;
       for (int round = 0, item = item_of_round(0); ok && item < n_items; item = item_of_round(++round)) {
-        const Item it = decode_item(item, args);
+        const Item it = decode_item<kGeneral>(item, args);
         if (it.n == 0) continue;
         const int slot = li & 1;
         if (li >= 2 && !mbar_wait(&bars->q_empty[slot], ((li >> 1) - 1) & 1, st, abort_flag, kSiteQEmpty)) break;
@@ -295,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int vt = 0;
       bool ok = true;
       for (int round = 0, item = item_of_round(0); ok && item < n_items; item = item_of_round(++round)) {
-        const Item it = decode_item(item, args);
+        const Item it = decode_item<kGeneral>(item, args);
         for (int j = 0; j < it.n; ++j, ++vt) {
           const int s = vt % SV, r = vt / SV;
           if (r > 0 && !mbar_wait(&bars->v_empty[s], (r - 1) & 1, st, abort_flag, kSiteVEmpty)) { ok = false; break; }
@@ -314,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------ S issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
-      Cursor sc;
+      Cursor<kGeneral> sc;
       sc.init(args, n_items);
       for (int ts = 0; sc.valid; ++ts, sc.next(args)) {
         const int buf = ts % kSBuf;
@@ -344,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------ P V issuer
     if (lane == 0) {
       constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
-      Cursor pc;
+      Cursor<kGeneral> pc;
       pc.init(args, n_items);
       for (int t = 0; pc.valid; ++t, pc.next(args)) {
         const int buf = t % kSBuf;
@@ -378,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l_g = 0.f;                             // this group's part of the row sum
     int my_item = -1;                            // item the group's (l_g, m_g) belong to
     int n_multi = 0;                             // items with >= 2 tiles completed so far
-    Cursor c;
+    Cursor<kGeneral> c;
     c.init(args, n_items);
     for (int t = 0; c.valid; ++t, c.next(args)) {
       const int j = c.j, n = c.it.n;
@@ -388,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((t & 1) != g) continue;                // the other group's tile
       const int buf = t % kSBuf;
       // Position of this thread's query among the keys.
-      const int qpos = (args.packed ? r % args.Nq : c.it.qbase + r) + (Nk - args.Nq);
+      const int qpos = kGeneral ? (args.packed ? r % args.Nq : c.it.qbase + r) + (Nk - args.Nq) : c.it.qbase + r;
       const uint32_t tS = tmem + buf * 128 + lane_off;
       if (!mbar_wait_warp(&bars->s_full[buf], (t / kSBuf) & 1, st, abort_flag, kSiteSFull)) break;
       tc_fence_after();
@@ -402,11 +408,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars->s_free[buf]);   // the MMA may compute S_{t+2} into this buffer now
 
       const int key0 = (c.it.j0 + j) * kBN;
+      const bool windowed = kGeneral && args.window > 0;
       if ((key0 + kBN > Nk) || (args.causal && key0 + kBN - 1 > c.it.qmin) ||
-          (args.window > 0 && key0 < c.it.qmax - args.window + 1)) {
+          (windowed && key0 < c.it.qmax - args.window + 1)) {
         // Keys [key0 + lo, key0 + hi) are visible to this row.
         const int hi = min(Nk, args.causal ? qpos + 1 : Nk) - key0;
-        const int lo = args.window > 0 ? qpos - args.window + 1 - key0 : 0;
+        const int lo = windowed ? qpos - args.window + 1 - key0 : 0;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -535,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
         const long long frow = c.it.row0 + r;
         if (r < c.it.rows) {
-          if (args.splits == 1) {
+          if (!kGeneral || args.splits == 1) {
             const float inv_l = 1.f / l_tot;
             __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.o) + frow * D;
 #pragma unroll
@@ -584,24 +591,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D>
+template <int D, bool kGeneral>
 static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const FwdArgs& a, const DevStatus& st, int num_sms, cudaStream_t stream) {
   using L = FwdCfg<D>;
   static_assert(L::kBytes <= 232448, "shared memory budget");
   static_assert(sizeof(Bars) <= 512, "barrier block");
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(fa_fwd_kernel<D, kGeneral>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const long long items = (long long)a.nqt * a.splits * a.units;
   const int grid = (int)(items < num_sms ? items : num_sms);
-  fa_fwd_kernel<D><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, a, st);
+  fa_fwd_kernel<D, kGeneral><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, a, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
                        const DevStatus& st, int num_sms, cudaStream_t stream) {
-  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, a, st, num_sms, stream);
-  return launch_fwd_d<128>(tq, tk, tv, a, st, num_sms, stream);
+  const bool general = a.Nq != a.Nk || a.window > 0 || a.splits > 1 || a.packed;
+  if (d == 64)
+    return general ? launch_fwd_d<64, true>(tq, tk, tv, a, st, num_sms, stream)
+                   : launch_fwd_d<64, false>(tq, tk, tv, a, st, num_sms, stream);
+  return general ? launch_fwd_d<128, true>(tq, tk, tv, a, st, num_sms, stream)
+                 : launch_fwd_d<128, false>(tq, tk, tv, a, st, num_sms, stream);
 }
 
 // Merge of the key splits ([Lecture] "推导 FlashAttention 的在线 softmax": both
