@@ -10,6 +10,12 @@ of the K timed steps (CUDA events around each step on the launching stream;
 L2 is flushed by a 256 MiB write between steps, outside the events).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --next     # the widened paths: decode (Nq << Nk) and window
+
+--next prints one JSON line per widened-path case (not the contract line):
+decode-shaped grouped attention (few query rows against a long key/value
+history, key splits + merge) against the HBM roofline, and sliding-window
+causal attention (forward and backward) in TFLOPS over the visible pairs.
 
 --impl reference times the CPU oracle (fp64 NumPy) on the host cores: each
 step is a bounded sample of the same workload (one block of query rows of one
@@ -64,6 +70,16 @@ def aggregate_tflops(step_flops: float, world: int, total_ms_max: float, steps: 
 # ---------------------------------------------------------------------------
 # measured peaks, kernel source hash, ncu traffic record
 # ---------------------------------------------------------------------------
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return 6800.0, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
 
 def bf16_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -429,6 +445,109 @@ def run_ours(args, w):
     return 0
 
 
+def _time_events(fn, steps, warmup, flush, stream):
+    """Mean device ms of fn over `steps` runs (CUDA events on `stream`), with an
+    L2 flush before each run outside the events."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    total = 0.0
+    for _ in range(steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        total += a.elapsed_time(b)
+    return total / steps
+
+
+def run_next(args):
+    """Measure the widened paths; one JSON line per case."""
+    import torch
+    import exact_io_aware_flashattention_gb300 as fa
+    from exact_io_aware_flashattention_gb300 import _build
+    _build.build()
+    fa.load_library()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    steps, warmup = max(args.steps, 20), max(args.warmup, 3)
+    hbm, hbm_src = hbm_peak()
+    peak, peak_src = bf16_peak()
+
+    def gen(shape, seed):
+        g = torch.Generator().manual_seed(seed)
+        return torch.randn(shape, generator=g).to(torch.bfloat16).to(dev)
+
+    # Decode: B=8, Hq=32, Hkv=8 (4 query heads per kv head), one new query row.
+    for Nk in (8192, 32768):
+        B, Hq, Hkv, Nq, d = 8, 32, 8, 1, 128
+        q, k, v = gen((B, Hq, Nq, d), 1), gen((B, Hkv, Nk, d), 2), gen((B, Hkv, Nk, d), 3)
+        splits = fa.fa_fwd_ex_default_splits(B, Hq, Hkv, Nq, Nk, d, 1, 0)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(1, fa.fa_fwd_ex_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, splits)), dtype=torch.uint8,
+                         device=dev)
+
+        def fn():
+            st = fa.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Nq,
+                              Nk, d, 1, 0, splits, d ** -0.5, ws.data_ptr(), ws.numel(), stream.cuda_stream)
+            if st != 0:
+                raise fa.FAError(st, "fa_fwd_ex")
+        ms = _time_events(fn, steps, warmup, flush, stream)
+        fa.check_device_status()
+        # Algorithmic bytes: K and V once (each kv head read once for its 4
+        # query heads), Q, O and LSE.
+        nbytes = 2 * B * Hkv * Nk * d * 2 + 2 * B * Hq * Nq * d * 2 + B * Hq * Nq * 4
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        print(json.dumps({"case": "decode", "metric": "decode attention HBM throughput", "value": gbs,
+                          "unit": "GB/s", "us": ms * 1e3, "dtype": "bf16", "data": "synthetic",
+                          "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "Nq": Nq, "Nk": Nk, "d": d, "causal": True,
+                                     "num_splits": splits, "l2": "flushed before each run"},
+                          "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                       "frac": gbs / hbm, "peak_source": hbm_src,
+                                       "algorithmic_bytes": nbytes}}), flush=True)
+
+    # Sliding window: B=2, H=16, N=8192, d=128, causal, window 1024.
+    B, Hq, Hkv, N, d, win = 2, 16, 16, 8192, 128, 1024
+    q, k, v, do = gen((B, Hq, N, d), 4), gen((B, Hkv, N, d), 5), gen((B, Hkv, N, d), 6), gen((B, Hq, N, d), 7)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, Hq, Hkv, N, d), dtype=torch.uint8, device=dev)
+    sh = stream.cuda_stream
+
+    def fwd():
+        st = fa.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, N, d,
+                          1, win, 1, d ** -0.5, None, 0, sh)
+        if st != 0:
+            raise fa.FAError(st, "fa_fwd_ex")
+
+    def bwd():
+        st = fa.fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, 1, win, d ** -0.5,
+                          ws.data_ptr(), ws.numel(), sh)
+        if st != 0:
+            raise fa.FAError(st, "fa_bwd_ex")
+    fwd()
+    ms_f = _time_events(fwd, steps, warmup, flush, stream)
+    ms_b = _time_events(bwd, steps, warmup, flush, stream)
+    fa.check_device_status()
+    pairs = sum(min(i + 1, win) for i in range(N))       # visible (query, key) pairs per head
+    ff = 4.0 * B * Hq * d * pairs
+    tf_f, tf_b = ff / (ms_f * 1e-3) / 1e12, 2.5 * ff / (ms_b * 1e-3) / 1e12
+    print(json.dumps({"case": "window", "metric": "sliding-window attention TFLOPS over visible pairs",
+                      "value": {"fwd": tf_f, "bwd": tf_b}, "unit": "TFLOPS",
+                      "ms": {"fwd": ms_f, "bwd": ms_b}, "dtype": "bf16", "data": "synthetic",
+                      "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "causal": True, "window": win,
+                                 "l2": "flushed before each run"},
+                      "frac_of_peak": {"fwd": tf_f / peak, "bwd": tf_b / peak}, "peak_source": peak_src}),
+          flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -437,7 +556,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--next", action="store_true", help="measure the widened paths (decode, window) instead")
     args = ap.parse_args()
+    if args.next:
+        return run_next(args)
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -342,13 +342,22 @@ int fa_fwd_ex_default_splits(int B, int Hq, int Hkv, int Nq, int Nk, int d, int 
   DeviceState* ds = nullptr;
   if (device_state(&ds) != FA_OK) return 1;
   const FwdGeometry g = fwd_geometry(B, Hq, Hkv, Nq, Nk, 1);
-  // Enough work items for about one per SM; each split keeps >= 4 key tiles.
-  long long units = (long long)g.units * g.nqt;
-  int s = (int)((ds->num_sms + units - 1) / units);
+  const long long units = (long long)g.units * g.nqt;
   int ntk = (Nk + 127) / 128;
   if (causal && window > 0) ntk = std::min(ntk, (window + 127) / 128 + 1);
-  s = std::min(s, std::max(1, ntk / 4));
-  return std::max(1, std::min(s, 64));
+  // Key tiles on the busiest SM, counting each item's fixed cost (its Q
+  // load, pipeline fill and epilogue) as about two key tiles.
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= std::min(64, ntk); ++s) {
+    const long long rounds = (units * s + ds->num_sms - 1) / ds->num_sms;
+    const long long cost = rounds * ((ntk + s - 1) / s + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
 }
 
 fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,

@@ -112,9 +112,10 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
 size_t fa_fwd_ex_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_splits);
 
 /*
- * A split count for fa_fwd_ex on the current device: enough work items for
- * about one per SM, at least 4 key tiles per split, at most 64 splits.
- * Returns 1 for problems that already fill the GPU (or invalid shapes).
+ * A split count for fa_fwd_ex on the current device: the count (1..64) that
+ * minimises the key tiles processed by the busiest SM, each work item
+ * costing about two key tiles extra.  Returns 1 for problems that already
+ * fill the GPU (or invalid shapes).
  */
 int fa_fwd_ex_default_splits(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window);
 
