@@ -96,6 +96,7 @@ def bf16_peak():
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ("fa_fwd.cu", "fa_internal.h", "sm103a.cuh"),
     "fa_bwd_dkdv_kernel": ("fa_bwd.cu", "fa_internal.h", "sm103a.cuh"),
+    "fa_bwd_dq_kernel": ("fa_bwd_dq.cu", "fa_internal.h", "sm103a.cuh"),
 }
 
 
@@ -527,7 +528,7 @@ def run_next(args):
 
     def bwd():
         st = fa.fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, 1, win, d ** -0.5,
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, 1, win, 0, d ** -0.5,
                           ws.data_ptr(), ws.numel(), sh)
         if st != 0:
             raise fa.FAError(st, "fa_bwd_ex")
@@ -544,6 +545,32 @@ def run_next(args):
                       "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "causal": True, "window": win,
                                  "l2": "flushed before each run"},
                       "frac_of_peak": {"fwd": tf_f / peak, "bwd": tf_b / peak}, "peak_source": peak_src}),
+          flush=True)
+
+    # Deterministic backward (separate dQ kernel) on the standard causal
+    # workload, against the reduce-add backward.
+    w = WORKLOADS[BENCH_WORKLOAD]
+    B, Hq, Hkv, N, d = w.B, w.Hq, w.Hkv, w.N, w.d
+    q, k, v, do = (t.to(dev) for t in make_workload_inputs(w))
+    o, lse = fa.forward(q, k, v, causal=True, scale=w.scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, Hq, Hkv, N, d), dtype=torch.uint8, device=dev)
+    res = {}
+    for det in (0, 1):
+        def bwd_det():
+            st = fa.fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, 1, 0, det, w.scale,
+                              ws.data_ptr(), ws.numel(), sh)
+            if st != 0:
+                raise fa.FAError(st, "fa_bwd_ex")
+        res[det] = _time_events(bwd_det, steps, warmup, flush, stream)
+    fa.check_device_status()
+    bf = 2.5 * 4.0 * B * Hq * N * N * d / 2
+    print(json.dumps({"case": "deterministic_backward", "metric": "backward TFLOPS (convention 2.5 x causal fwd)",
+                      "value": {"deterministic": bf / (res[1] * 1e-3) / 1e12,
+                                "reduce_add": bf / (res[0] * 1e-3) / 1e12},
+                      "unit": "TFLOPS", "ms": {"deterministic": res[1], "reduce_add": res[0]}, "dtype": "bf16",
+                      "data": "synthetic", "config": {"workload": w.name, "l2": "flushed before each run"}}),
           flush=True)
     return 0
 

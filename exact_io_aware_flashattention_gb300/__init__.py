@@ -60,7 +60,7 @@ _SIGNATURES = {
     "fa_fwd_ex": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p, _sz, _p], _i),
     "fa_fwd_ex_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
     "fa_fwd_ex_default_splits": ([_i, _i, _i, _i, _i, _i, _i, _i], _i),
-    "fa_bwd_ex": ([_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _sz, _p], _i),
+    "fa_bwd_ex": ([_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p, _sz, _p], _i),
     "fa_bwd_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
     "fa_bwd": ([_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p, _sz, _p], _i),
     "fa_bwd_preprocess": ([_p, _p, _p, _i, _i, _i, _i, _i, _p, _sz, _p], _i),
@@ -128,10 +128,10 @@ def fa_fwd_ex_default_splits(B, Hq, Hkv, Nq, Nk, d, causal, window):
     return load_library().fa_fwd_ex_default_splits(B, Hq, Hkv, Nq, Nk, d, int(causal), int(window))
 
 
-def fa_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, window, scale, workspace,
+def fa_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, window, deterministic, scale, workspace,
               workspace_bytes, stream):
     return load_library().fa_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, int(causal), int(window),
-                                    float(scale), workspace, workspace_bytes, stream)
+                                    int(deterministic), float(scale), workspace, workspace_bytes, stream)
 
 
 def fa_bwd_workspace_bytes(B, Hq, Hkv, N, d):
@@ -278,7 +278,7 @@ def workspace_for(B, Hq, Hkv, N, d, device):
 
 
 def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, workspace=None,
-             dq=None, dk=None, dv=None, stream=None, window: int = 0):
+             dq=None, dk=None, dv=None, stream=None, window: int = 0, deterministic: bool = False):
     """dQ, dK, dV of sum(dO * O), recomputing P from the forward's LSE."""
     import torch
     B, Hq, N, d = q.shape
@@ -294,7 +294,7 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     _raise(fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, causal, window, scale,
+                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, causal, window, deterministic, scale,
                      workspace.data_ptr(), workspace.numel(), _stream_handle(stream)), "fa_bwd_ex")
     return dq, dk, dv
 

@@ -21,7 +21,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_bwd_dq.cu"]
 HEADERS = ["sm103a.cuh", "fa_internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

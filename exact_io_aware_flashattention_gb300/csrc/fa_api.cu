@@ -260,8 +260,8 @@ fa_status validate_dkdv(const void* q, const void* k, const void* v, const void*
 }
 
 fa_status dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B, int Hq, int Hkv,
-               int N, int d, int causal, int window, float scale, void* workspace, size_t workspace_bytes,
-               void* stream) {
+               int N, int d, int causal, int window, int with_dq, float scale, void* workspace,
+               size_t workspace_bytes, void* stream) {
   FA_TRY(validate_dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
   DeviceState* ds = nullptr;
   FA_TRY(device_state(&ds));
@@ -285,6 +285,7 @@ fa_status dkdv(const void* q, const void* k, const void* v, const void* dO, void
   a.N = N;
   a.causal = causal;
   a.window = window;
+  a.with_dq = with_dq;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_status(
@@ -441,7 +442,7 @@ fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, int
 fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B, int Hq,
                       int Hkv, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
                       void* stream) {
-  return dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, 0, scale, workspace, workspace_bytes, stream);
+  return dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, 0, 1, scale, workspace, workspace_bytes, stream);
 }
 
 
@@ -466,15 +467,15 @@ fa_status fa_bwd_dq_convert(void* dq, int B, int Hq, int Hkv, int N, int d, floa
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                  void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                  void* workspace, size_t workspace_bytes, void* stream) {
-  return fa_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, 0, scale, workspace, workspace_bytes,
-                   stream);
+  return fa_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, 0, 0, scale, workspace,
+                   workspace_bytes, stream);
 }
 
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                     void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, int window,
-                    float scale, void* workspace, size_t workspace_bytes, void* stream) {
+                    int deterministic, float scale, void* workspace, size_t workspace_bytes, void* stream) {
   if (!o || !dq || !lse) return FA_ERR_NULL_PTR;
-  if (window < 0 || (window > 0 && !causal)) return FA_ERR_BAD_ARGUMENT;
+  if (window < 0 || (window > 0 && !causal) || (deterministic != 0 && deterministic != 1)) return FA_ERR_BAD_ARGUMENT;
   FA_TRY(validate_dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
   if (!aligned16(o) || !aligned16(dq) || !aligned16(lse)) return FA_ERR_MISALIGNED;
   const size_t qb = elems(B, Hq, N, d) * 2, kb = elems(B, Hkv, N, d) * 2;
@@ -488,9 +489,40 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
   const Range rl = range(lse, (size_t)B * Hq * N * 4), rw = range(workspace, ws_layout(B, Hq, N, d).total);
   if (overlap(ro, range(dk, kb)) || overlap(ro, range(dv, kb)) || overlap(ro, rw)) return FA_ERR_ALIASING;
   if (overlap(rl, range(dk, kb)) || overlap(rl, range(dv, kb)) || overlap(rl, rw)) return FA_ERR_ALIASING;
-  FA_TRY(fa_bwd_preprocess(o, dO, lse, B, Hq, Hkv, N, d, workspace, workspace_bytes, stream));
-  FA_TRY(dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, window, scale, workspace, workspace_bytes, stream));
-  return fa_bwd_dq_convert(dq, B, Hq, Hkv, N, d, scale, workspace, workspace_bytes, stream);
+  if (!deterministic) {
+    FA_TRY(fa_bwd_preprocess(o, dO, lse, B, Hq, Hkv, N, d, workspace, workspace_bytes, stream));
+    FA_TRY(dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, window, 1, scale, workspace, workspace_bytes, stream));
+    return fa_bwd_dq_convert(dq, B, Hq, Hkv, N, d, scale, workspace, workspace_bytes, stream);
+  }
+  // Deterministic: LSE*log2(e) and D only (no accumulator), dK/dV without
+  // dQ partials, then dQ per query tile in a fixed order.
+  DeviceState* ds = nullptr;
+  FA_TRY(device_state(&ds));
+  const WsLayout w = ws_layout(B, Hq, N, d);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  FA_TRY(launch_status(fa::launch_bwd_preprocess(d, o, dO, lse, reinterpret_cast<float*>(ws + w.lse2_off),
+                                                 reinterpret_cast<float*>(ws + w.dr_off), nullptr, (long long)B * Hq,
+                                                 N, ds->num_sms, st)));
+  FA_TRY(dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, window, 0, scale, workspace, workspace_bytes, stream));
+  CUtensorMap tq, tk, tv, tdo;
+  FA_TRY(tmap_bf16(&tq, q, B, Hq, N, d));
+  FA_TRY(tmap_bf16(&tk, k, B, Hkv, N, d));
+  FA_TRY(tmap_bf16(&tv, v, B, Hkv, N, d));
+  FA_TRY(tmap_bf16(&tdo, dO, B, Hq, N, d));
+  fa::DqArgs a;
+  a.lse2 = reinterpret_cast<const float*>(ws + w.lse2_off);
+  a.drow = reinterpret_cast<const float*>(ws + w.dr_off);
+  a.dq = dq;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.N = N;
+  a.causal = causal;
+  a.window = window;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  return launch_status(fa::launch_bwd_dq(d, tq, tk, tv, tdo, a, dev_status(ds), st));
 }
 
 fa_status fa_last_device_status(void* stream, int* detail) {

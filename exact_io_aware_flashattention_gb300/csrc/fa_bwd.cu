@@ -83,7 +83,10 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
-template <int D>
+// kDq = false: dK and dV only (the deterministic backward computes dQ in its
+// own kernel): no dQ MMA, no dS tile in shared memory, no dQ staging or
+// reduce-adds; the store warp idles.
+template <int D, bool kDq>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -123,9 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->kv_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->q_full[s], 1);
-      mbar_init(&bars->q_empty[s], 2);   // dK/dQ MMAs done + dQ staging read by TMA
+      mbar_init(&bars->q_empty[s], kDq ? 2 : 1);   // dK/dQ MMAs done (+ dQ staging read by TMA)
       mbar_init(&bars->do_full[s], 1);
-      mbar_init(&bars->do_empty[s], 2);  // dP/dV MMAs done + dQ staging read by TMA
+      mbar_init(&bars->do_empty[s], kDq ? 2 : 1);  // dP/dV MMAs done (+ dQ staging read by TMA)
       mbar_init(&bars->ld_full[s], 1);
       mbar_init(&bars->ld_empty[s], 256);
       for (int g = 0; g < 2; ++g) mbar_init(&bars->st_full[s][g], 128);
@@ -251,7 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tS, desc_kmajor(sK, k16, kBlockBytes), desc_kmajor(qa, k16, kBlockBytes), idSS, k16 > 0);
         mma_commit(&bars->s_full);
         if (!mbar_wait(&bars->do_full[slot], sph, st, abort_flag, kSiteDoFull)) break;
-        if (t > 0 && !mbar_wait(&bars->dq_empty, pph, st, abort_flag, kSiteDqEmpty)) break;
+        // dP_t overwrites the dQ partial of item t-1 (read out by then) or,
+        // without dQ, dP^T of item t-1 (read before ds_full of t-1).
+        if (kDq && t > 0 && !mbar_wait(&bars->dq_empty, pph, st, abort_flag, kSiteDqEmpty)) break;
         tc_fence_after();
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
@@ -274,11 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tDK, tS + (k16 >> 2) * 64 + 32 + (k16 & 3) * 8, desc_mnmajor(qa, k16, kBlockBytes), idKM,
                       (t > 0 || k16 > 0) ? 1u : 0u);
         mma_commit(&bars->dk_done);
+        if (kDq) {
 #pragma unroll
-        for (int k16 = 0; k16 < kT / 16; ++k16)
-          mma_bf16_ss(tDP, desc_mnmajor(sDS, k16, kBlockBytes), desc_mnmajor(sK, k16, kBlockBytes), idMM,
-                      k16 > 0 ? 1u : 0u);
-        mma_commit(&bars->dq_full);
+          for (int k16 = 0; k16 < kT / 16; ++k16)
+            mma_bf16_ss(tDP, desc_mnmajor(sDS, k16, kBlockBytes), desc_mnmajor(sK, k16, kBlockBytes), idMM,
+                        k16 > 0 ? 1u : 0u);
+          mma_commit(&bars->dq_full);
+        }
         mma_commit(&bars->q_empty[slot]);
       }
       mma_commit(&bars->dkv_done);
@@ -378,16 +385,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // operand of dK) and this group's 64-column block of the shared tile
       // (the A operand of dQ).
       tmem_st32(tS + lane_off + c0 + 32, ds);
+      if (kDq) {
 #pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16)
-        st_shared_v4(sDS + g * kBlockBytes + swz128(r, c16), ds[c16 * 4], ds[c16 * 4 + 1], ds[c16 * 4 + 2],
-                     ds[c16 * 4 + 3]);
-      fence_proxy_async_smem();
+        for (int c16 = 0; c16 < 8; ++c16)
+          st_shared_v4(sDS + g * kBlockBytes + swz128(r, c16), ds[c16 * 4], ds[c16 * 4 + 1], ds[c16 * 4 + 2],
+                       ds[c16 * 4 + 3]);
+        fence_proxy_async_smem();
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->ds_full);
       mbar_arrive(&bars->ld_empty[slot]);
 
+      if (!kDq) continue;
       if (!mbar_wait_warp(&bars->dq_full, ph, st, abort_flag, kSiteDqFull)) { ok = false; break; }
       tc_fence_after();
       // dQ partial row r (a query) x this group's head-dim columns: read it out
@@ -453,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (rows past N are clipped by the tensor map), and hand the item's dO and
     // Q slots back to the producer once TMA has read the staging.  Waiting
     // for those reads here keeps them off the compute warps.
-    if (lane == 0) {
+    if (kDq && lane == 0) {
       for (int t = 0; t < n_items; ++t) {
         const int slot = t & 1;
         const int head = b * args.Hq + kvh * G + t / nqi;
@@ -530,6 +540,7 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __r
       lse2[prow] = valid ? lse[row] * kLog2e : INFINITY;
     }
   }
+  if (dq_accum == nullptr) return;   // no accumulator (deterministic dQ)
   const long long n4 = heads * N * (D / 4);
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride)
     dq_accum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -552,7 +563,7 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float4* __
 
 }  // namespace
 
-template <int D>
+template <int D, bool kDq>
 static cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, const DevStatus& st,
                                  cudaStream_t stream) {
@@ -560,19 +571,23 @@ static cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, c
   static_assert(L::kBytes <= 232448, "shared memory budget");
   static_assert(sizeof(Bars) <= 256, "barrier block");
   cudaError_t e =
-      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, kDq>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const int nt = (a.N + kT - 1) / kT;
   dim3 grid(a.Hkv, a.B, nt);
-  fa_bwd_dkdv_kernel<D><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, a, st);
+  fa_bwd_dkdv_kernel<D, kDq><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, a, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, const DevStatus& st,
                             cudaStream_t stream) {
-  if (d == 64) return launch_dkdv_d<64>(tq, tk, tv, tdo, tdq, a, st, stream);
-  return launch_dkdv_d<128>(tq, tk, tv, tdo, tdq, a, st, stream);
+  if (a.with_dq) {
+    if (d == 64) return launch_dkdv_d<64, true>(tq, tk, tv, tdo, tdq, a, st, stream);
+    return launch_dkdv_d<128, true>(tq, tk, tv, tdo, tdq, a, st, stream);
+  }
+  if (d == 64) return launch_dkdv_d<64, false>(tq, tk, tv, tdo, tdq, a, st, stream);
+  return launch_dkdv_d<128, false>(tq, tk, tv, tdo, tdq, a, st, stream);
 }
 
 static int grid_for(long long work_items, int num_sms) {

@@ -1,0 +1,355 @@
+// Deterministic dQ for the attention backward: one CTA per 128-row query tile
+// of one (head, batch) walks the key tiles the tile can see and accumulates
+// dQ = scale * sum_j dS_j K_j in tensor memory, in a fixed order, so dQ is
+// bitwise reproducible (the dK/dV kernel then runs without its dQ partials).
+// It recomputes what the dK/dV kernel recomputes, from the saved LSE
+// ([FA-memory] "38.解释FlashAttention的显存优化原理", part 2(2); [QBank-36]
+// part 7), with queries instead of keys on the tensor-memory lanes:
+//   S = Q K_j^T, P = 2^(S * scale * log2 e - LSE * log2 e),
+//   dP = dO V_j^T, dS = P (dP - D), dQ += dS K_j.
+//
+// CTA layout (320 threads):
+//   warp 0      TMA producer: Q, dO and the tile's 128 LSE / D values once,
+//               K and V per key tile (rings of kStages)
+//   warp 1      TMEM allocator and MMA issuer
+//   warps 2-9   two compute warpgroups: thread t of a group owns query row t
+//               (TMEM lane t); group g handles key columns [64g, 64g+64) of S
+//               and dP and head-dim columns [g d/2, (g+1) d/2) of the output.
+// Tensor memory: two S buffers (0, 128), dP at 256, dQ at 384.  dS (bf16) is
+// written over each group's own first 32 columns of its S buffer and read
+// there by the dQ MMA.  Tensor pipe order: S_0 dP_0 | S_1 dP_1 dQ_0 | S_2 dP_2
+// dQ_1 ...  S_{j+2} reuses S buffer j % 2 once dQ_j has read dS_j from it;
+// dP_{j+1} waits until the compute threads have read dP_j.
+#include "fa_internal.h"
+#include "sm103a.cuh"
+
+namespace fa {
+
+namespace {
+
+constexpr int kT = 128;
+constexpr int kThreads = 320;
+constexpr uint32_t kBlockBytes = 128u * 128u;
+
+template <int D>
+struct DqSmem {
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr uint32_t kTile = 128u * D * 2u;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kDO = kQ + kTile;
+  static constexpr uint32_t kK = kDO + kTile;                 // kStages
+  static constexpr uint32_t kV = kK + kStages * kTile;        // kStages
+  static constexpr uint32_t kLse = kV + kStages * kTile;      // 128 fp32
+  static constexpr uint32_t kDr = kLse + 512u;                // 128 fp32
+  static constexpr uint32_t kBar = kDr + 512u;
+  static constexpr uint32_t kBytes = kBar + 256u;
+};
+
+enum : int {
+  kSiteQ = 41, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteSFull, kSiteDpFull, kSiteDpFree,
+  kSiteDsFull, kSiteDqDone, kSiteDqFinal
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], ds_full[2], dq_done[2];
+  uint64_t dp_full, dp_free, dq_final, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                     const DqArgs args, const DevStatus st) {
+  using L = DqSmem<D>;
+  constexpr int kAtoms = D / 64;
+  constexpr int SK = L::kStages;
+  constexpr int kHalfD = D / 2;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Bars* bars = reinterpret_cast<Bars*>(smem + L::kBar);
+  volatile int* abort_flag = &bars->abort;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(st, kErrDeviceTimeout, 40);
+    return;
+  }
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = args.N;
+  const int nt = (N + kT - 1) / kT;
+  const int h = blockIdx.x;
+  const int b = blockIdx.y;
+  const int i = nt - 1 - (int)blockIdx.z;        // query tile (heaviest causal tiles launched first)
+  const int kvh = h / (args.Hq / args.Hkv);
+  // Key tiles [jlo, jhi) hold keys some row of this tile may see.
+  const int jhi = args.causal ? i + 1 : nt;
+  const int jlo = args.window > 0 ? max(0, i * kT - args.window + 1) / kT : 0;
+  const int n = jhi - jlo;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < SK; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars->s_full[x], 1);
+      mbar_init(&bars->ds_full[x], 256);
+      mbar_init(&bars->dq_done[x], 1);
+    }
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->dp_free, 256);
+    mbar_init(&bars->dq_final, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    mbar_fence_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmDO);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const uint32_t tDP = tmem + 256, tDQ = tmem + 384;
+  const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
+  const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
+  const int ntp = nt * kT;                       // padded rows per head of the LSE / D arrays
+  const size_t roff = ((size_t)b * args.Hq + h) * ntp + (size_t)i * kT;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars->q_full, 2 * L::kTile + 1024u);
+      for (int a = 0; a < kAtoms; ++a) {
+        tma_load_4d(smem + L::kQ + a * kBlockBytes, &tmQ, &bars->q_full, a * 64, i * kT, h, b);
+        tma_load_4d(smem + L::kDO + a * kBlockBytes, &tmDO, &bars->q_full, a * 64, i * kT, h, b);
+      }
+      bulk_load(smem + L::kLse, args.lse2 + roff, 512u, &bars->q_full);
+      bulk_load(smem + L::kDr, args.drow + roff, 512u, &bars->q_full);
+      int issued = 0;
+      for (int jj = 0; jj < n; ++jj, ++issued) {
+        const int s = jj % SK, r = jj / SK;
+        if (r > 0 && !mbar_wait(&bars->k_empty[s], (r - 1) & 1, st, abort_flag, kSiteKEmpty)) break;
+        mbar_arrive_expect_tx(&bars->k_full[s], L::kTile);
+        for (int a = 0; a < kAtoms; ++a)
+          tma_load_4d(smem + L::kK + s * L::kTile + a * kBlockBytes, &tmK, &bars->k_full[s], a * 64,
+                      (jlo + jj) * kT, kvh, b);
+        if (r > 0 && !mbar_wait(&bars->v_empty[s], (r - 1) & 1, st, abort_flag, kSiteVEmpty)) {
+          ++issued;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars->v_full[s], L::kTile);
+        for (int a = 0; a < kAtoms; ++a)
+          tma_load_4d(smem + L::kV + s * L::kTile + a * kBlockBytes, &tmV, &bars->v_full[s], a * 64,
+                      (jlo + jj) * kT, kvh, b);
+      }
+      // Every copy issued must have landed before the CTA may exit.
+      mbar_wait_drain(&bars->q_full, 0, st.timeout_ns);
+      for (int s = 0; s < SK && s < issued; ++s) {
+        const int last = issued - 1 - ((issued - 1 - s) % SK);
+        mbar_wait_drain(&bars->k_full[s], (last / SK) & 1, st.timeout_ns);
+        mbar_wait_drain(&bars->v_full[s], (last / SK) & 1, st.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);   // S, dP
+      constexpr uint32_t idQ = idesc_bf16(128, D, false, true);       // dQ += dS K (K as the MN-major operand)
+      // dQ_j: A = dS_j in S buffer j % 2 (group g's keys at columns 64g..),
+      // B = K_j; releases the K stage afterwards.
+      auto issue_dq = [&](int jj) -> bool {
+        const int x = jj & 1, s = jj % SK;
+        if (!mbar_wait(&bars->ds_full[x], (jj >> 1) & 1, st, abort_flag, kSiteDsFull)) return false;
+        tc_fence_after();
+        const uint32_t ka = sK + s * L::kTile;
+#pragma unroll
+        for (int k16 = 0; k16 < kT / 16; ++k16)
+          mma_bf16_ts(tDQ, tmem + x * 128 + (k16 >> 2) * 64 + (k16 & 3) * 8, desc_mnmajor(ka, k16, kBlockBytes),
+                      idQ, (jj > 0 || k16 > 0) ? 1u : 0u);
+        mma_commit(&bars->dq_done[x]);
+        mma_commit(&bars->k_empty[s]);
+        return true;
+      };
+      bool ok = mbar_wait(&bars->q_full, 0, st, abort_flag, kSiteQ);
+      for (int jj = 0; ok && jj < n; ++jj) {
+        const int x = jj & 1, s = jj % SK;
+        // S_jj overwrites dS_{jj-2} (read by dQ_{jj-2}).
+        if (jj >= 2 && !mbar_wait(&bars->dq_done[x], ((jj - 2) >> 1) & 1, st, abort_flag, kSiteDqDone)) break;
+        if (!mbar_wait(&bars->k_full[s], (jj / SK) & 1, st, abort_flag, kSiteKFull)) break;
+        tc_fence_after();
+        const uint32_t ka = sK + s * L::kTile;
+#pragma unroll
+        for (int k16 = 0; k16 < D / 16; ++k16)
+          mma_bf16_ss(tmem + x * 128, desc_kmajor(sQ, k16, kBlockBytes), desc_kmajor(ka, k16, kBlockBytes), idSS,
+                      k16 > 0);
+        mma_commit(&bars->s_full[x]);
+        // dP_jj overwrites dP_{jj-1}: the compute threads must have read it.
+        if (jj >= 1 && !mbar_wait(&bars->dp_free, (jj - 1) & 1, st, abort_flag, kSiteDpFree)) break;
+        if (!mbar_wait(&bars->v_full[s], (jj / SK) & 1, st, abort_flag, kSiteVFull)) break;
+        tc_fence_after();
+        const uint32_t va = sV + s * L::kTile;
+#pragma unroll
+        for (int k16 = 0; k16 < D / 16; ++k16)
+          mma_bf16_ss(tDP, desc_kmajor(sDO, k16, kBlockBytes), desc_kmajor(va, k16, kBlockBytes), idSS, k16 > 0);
+        mma_commit(&bars->dp_full);
+        mma_commit(&bars->v_empty[s]);
+        if (jj >= 1 && !issue_dq(jj - 1)) break;
+        if (jj == n - 1) ok = issue_dq(jj);
+      }
+      mma_commit(&bars->dq_final);
+      mma_commit(&bars->drain);
+      mbar_wait_drain(&bars->drain, 0, st.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    const int g = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int q = i * kT + r;                      // this thread's query
+    const float sl2 = args.scale_log2;
+    const uint64_t sl2x2 = f2pack(sl2, sl2);
+    bool ok = mbar_wait_warp(&bars->q_full, 0, st, abort_flag, kSiteQ);
+    // Rows past N have LSE*log2(e) = +inf in the padded array: P = 0.
+    const float lse2 = ok ? reinterpret_cast<const float*>(smem + L::kLse)[r] : 0.f;
+    const float drow = ok ? reinterpret_cast<const float*>(smem + L::kDr)[r] : 0.f;
+    const uint64_t nl2 = f2pack(-lse2, -lse2);
+    const uint64_t nd2 = f2pack(-drow, -drow);
+    for (int jj = 0; ok && jj < n; ++jj) {
+      const int x = jj & 1;
+      const int j = jlo + jj;
+      if (!mbar_wait_warp(&bars->s_full[x], (jj >> 1) & 1, st, abort_flag, kSiteSFull)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tS = tmem + x * 128 + lane_off + g * 64;
+      uint32_t pr[2][32];
+      tmem_ld32(tS, pr[0]);
+      tmem_ld32(tS + 32, pr[1]);
+      tmem_wait_ld();
+      reg_fence(pr[0]);
+      reg_fence(pr[1]);
+      // Visible key columns of this group: [clo, chi) (causal: key <= q;
+      // window: key > q - w; keys past N never).
+      const int kc0 = j * kT + g * 64;             // key of the group's column 0
+      int chi = min(64, N - kc0);
+      if (args.causal) chi = min(chi, q + 1 - kc0);
+      const int clo = args.window > 0 ? max(0, q - args.window + 1 - kc0) : 0;
+#pragma unroll
+      for (int hq = 0; hq < 2; ++hq) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int col = hq * 32 + e;
+          float lo, hi;
+          f2unpack(ffma2(f2pack(__uint_as_float(pr[hq][e]), __uint_as_float(pr[hq][e + 1])), sl2x2, nl2), lo, hi);
+          lo = (col >= clo && col < chi) ? ex2(lo) : 0.f;
+          hi = (col + 1 >= clo && col + 1 < chi) ? ex2(hi) : 0.f;
+          pr[hq][e] = __float_as_uint(lo);
+          pr[hq][e + 1] = __float_as_uint(hi);
+        }
+      }
+      if (!mbar_wait_warp(&bars->dp_full, jj & 1, st, abort_flag, kSiteDpFull)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t dp[2][32];
+      tmem_ld32(tDP + lane_off + g * 64, dp[0]);
+      tmem_ld32(tDP + lane_off + g * 64 + 32, dp[1]);
+      tmem_wait_ld();
+      reg_fence(dp[0]);
+      reg_fence(dp[1]);
+      tc_fence_before();
+      mbar_arrive(&bars->dp_free);
+      uint32_t ds[32];
+#pragma unroll
+      for (int hq = 0; hq < 2; ++hq) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float a0, a1;
+          f2unpack(fmul2(f2pack(__uint_as_float(pr[hq][e]), __uint_as_float(pr[hq][e + 1])),
+                         fadd2(f2pack(__uint_as_float(dp[hq][e]), __uint_as_float(dp[hq][e + 1])), nd2)),
+                   a0, a1);
+          ds[hq * 16 + e / 2] = cvt_bf16x2(a0, a1);
+        }
+      }
+      // dS (bf16) over this group's own first 32 columns of the S buffer,
+      // already read into registers: the A operand of dQ_jj.
+      tmem_st32(tS, ds);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_full[x]);
+    }
+
+    if (ok && mbar_wait_warp(&bars->dq_final, 0, st, abort_flag, kSiteDqFinal)) {
+      tc_fence_after();
+      __nv_bfloat16* dst =
+          reinterpret_cast<__nv_bfloat16*>(args.dq) + (((size_t)b * args.Hq + h) * N + (size_t)q) * D + g * kHalfD;
+#pragma unroll
+      for (int c = 0; c < kHalfD / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tDQ + lane_off + g * kHalfD + c * 32, v);
+        tmem_wait_ld();
+        reg_fence(v);
+        if (q < N) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = cvt_bf16x2(__uint_as_float(v[u * 8 + 0]) * args.scale, __uint_as_float(v[u * 8 + 1]) * args.scale);
+            w.y = cvt_bf16x2(__uint_as_float(v[u * 8 + 2]) * args.scale, __uint_as_float(v[u * 8 + 3]) * args.scale);
+            w.z = cvt_bf16x2(__uint_as_float(v[u * 8 + 4]) * args.scale, __uint_as_float(v[u * 8 + 5]) * args.scale);
+            w.w = cvt_bf16x2(__uint_as_float(v[u * 8 + 6]) * args.scale, __uint_as_float(v[u * 8 + 7]) * args.scale);
+            *reinterpret_cast<uint4*>(dst + c * 32 + u * 8) = w;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+template <int D>
+static cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, cudaStream_t stream) {
+  using L = DqSmem<D>;
+  static_assert(L::kBytes <= 232448, "shared memory budget");
+  static_assert(sizeof(Bars) <= 256, "barrier block");
+  cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  if (e != cudaSuccess) return e;
+  const int nt = (a.N + kT - 1) / kT;
+  dim3 grid(a.Hq, a.B, nt);
+  fa_bwd_dq_kernel<D><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, a, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, cudaStream_t stream) {
+  if (d == 64) return launch_dq_d<64>(tq, tk, tv, tdo, a, st, stream);
+  return launch_dq_d<128>(tq, tk, tv, tdo, a, st, stream);
+}
+
+}  // namespace fa

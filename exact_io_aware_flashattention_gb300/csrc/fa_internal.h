@@ -35,9 +35,24 @@ struct BwdArgs {
   int B, Hq, Hkv, N;
   int causal;
   int window;         // > 0: key j visible to query i only if j > i - window (with causal)
+  int with_dq;        // 1: also add the dQ partials into dq_accum; 0: dK, dV only
   float scale;        // softmax scale
   float scale_log2;   // scale * log2(e)
 };
+
+struct DqArgs {
+  const float* lse2;  // [B*Hq, ntp] fp32, LSE * log2(e), padded (workspace)
+  const float* drow;  // [B*Hq, ntp] fp32, rowsum(dO * O), padded (workspace)
+  void* dq;           // [B, Hq, N, d] bf16
+  int B, Hq, Hkv, N;
+  int causal, window;
+  float scale;
+  float scale_log2;
+};
+
+// Deterministic dQ: one CTA per query tile, fixed accumulation order.
+cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, cudaStream_t stream);
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
                        const DevStatus& st, int num_sms, cudaStream_t stream);

@@ -142,16 +142,26 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * fa_bwd with a sliding window (see fa_fwd_ex): window = w >= 1 with causal
- * = 1 recomputes P with key j visible to query i iff i - w < j <= i, and
- * only visits the (query tile, key tile) pairs inside that band; window = 0
- * is fa_bwd.  Self-attention only (Nq == Nk == N).  FA_ERR_BAD_ARGUMENT for
- * window < 0 or window > 0 without causal; otherwise as fa_bwd.  o and lse
- * must come from the forward with the same window.
+ * fa_bwd with two options.
+ *   window = w >= 1 with causal = 1: P is recomputed with key j visible to
+ *     query i iff i - w < j <= i (the sliding window of fa_fwd_ex), and only
+ *     the (query tile, key tile) pairs inside that band are visited;
+ *     window = 0 is plain causal / full attention.  o and lse must come from
+ *     the forward with the same window.  Self-attention only (Nq == Nk == N).
+ *   deterministic = 1: dQ is accumulated per 128-row query tile by a separate
+ *     kernel that walks the key tiles in a fixed order, so dQ (like dK, dV,
+ *     always) is bitwise reproducible from run to run; it costs the S and dP
+ *     recomputation a second time (3 more MMAs per tile pair, against 1 dQ
+ *     MMA and the fp32 reduction saved).  deterministic = 0 adds the key
+ *     tiles' dQ partials into an fp32 accumulator in arrival order (faster,
+ *     reproducible only up to rounding).  Same workspace either way.
+ * FA_ERR_BAD_ARGUMENT for window < 0, window > 0 without causal, or
+ * deterministic not 0/1; otherwise as fa_bwd.  fa_bwd is
+ * fa_bwd_ex(..., window = 0, deterministic = 0, ...).
  */
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                     void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, int window,
-                    float scale, void* workspace, size_t workspace_bytes, void* stream);
+                    int deterministic, float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Backward step 1: D = rowsum(dO * O) and LSE * log2(e) into the workspace

@@ -152,9 +152,11 @@ def test_fwd_ex_workspace_formula(lib):
 @pytest.mark.parametrize("kw,status", [
     (dict(window=-1), fa.FA_ERR_BAD_ARGUMENT),
     (dict(window=8, causal=0), fa.FA_ERR_BAD_ARGUMENT),
+    (dict(deterministic=2), fa.FA_ERR_BAD_ARGUMENT),
 ])
 def test_bwd_ex_rejects_bad_window(lib, kw, status):
     args = dict(q=A, k=2 * A, v=3 * A, o=4 * A, do=5 * A, lse=6 * A, dq=7 * A, dk=8 * A, dv=9 * A, B=1, Hq=1, Hkv=1,
-                N=16, d=64, causal=1, window=0, scale=0.125, workspace=10 * A, workspace_bytes=1 << 20, stream=None)
+                N=16, d=64, causal=1, window=0, deterministic=0, scale=0.125, workspace=10 * A, workspace_bytes=1 << 20,
+                stream=None)
     args.update(kw)
     assert fa.fa_bwd_ex(**args) == status

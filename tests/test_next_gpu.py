@@ -101,3 +101,44 @@ def test_splits_agree_with_one_pass(cuda_lib):
     torch.cuda.synchronize()
     assert (o1.float() - o4.float()).abs().max() <= 1e-2
     assert (l1 - l4).abs().max() <= 1e-4 * max(1.0, l1.abs().max().item())
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,causal,window", [
+    (1, 2, 1, 300, 64, True, 0),
+    (2, 4, 2, 1000, 128, True, 0),
+    (1, 4, 4, 513, 128, False, 0),
+    (1, 2, 2, 700, 64, True, 150),
+    (1, 8, 2, 129, 128, True, 1),
+])
+def test_deterministic_backward(cuda_lib, B, Hq, Hkv, N, d, causal, window):
+    q, k, v, do = make_qkvdo(B, Hq, Hkv, N, d, seed=N * 3 + d + window)
+    scale = d ** -0.5
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = fa.forward_ex(qd, kd, vd, causal=causal, scale=scale, window=window)
+    g1 = fa.backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale, window=window, deterministic=True)
+    g2 = fa.backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale, window=window, deterministic=True)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    # Bitwise reproducible, dQ included.
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+    rdq, rdk, rdv = ref.attention_backward(f64(q), f64(k), f64(v), f64(do), causal, scale, window=window)
+    assert_bwd(*g1, rdq, rdk, rdv, f"deterministic N={N} window={window}")
+    # Same dK, dV as the reduce-add backward (identical MMAs); dQ within rounding.
+    g3 = fa.backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale, window=window)
+    torch.cuda.synchronize()
+    assert torch.equal(g1[1], g3[1]) and torch.equal(g1[2], g3[2])
+    assert (g1[0].float() - g3[0].float()).abs().max() <= 2e-2
+
+
+def test_deterministic_backward_standard_workload(cuda_lib):
+    from exact_io_aware_flashattention_gb300.inputs import WORKLOADS, make_workload_inputs
+    w = WORKLOADS["causal_b4_h16_n2048_d128"]
+    q, k, v, do = make_workload_inputs(w)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, causal=True, scale=w.scale)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, causal=True, scale=w.scale, deterministic=True)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    rdq, rdk, rdv = ref.attention_backward(f64(q), f64(k), f64(v), f64(do), True, w.scale)
+    assert_bwd(dq, dk, dv, rdq, rdk, rdv, "deterministic standard causal workload")
