@@ -289,7 +289,7 @@ fa_status dkdv(const void* q, const void* k, const void* v, const void* dO, void
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_status(
-      fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, tdq, a, dev_status(ds), static_cast<cudaStream_t>(stream)));
+      fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, tdq, a, dev_status(ds), ds->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace

@@ -7,9 +7,11 @@
 //   1. preprocess: D_i = sum_c dO[i,c] * O[i,c] (warp-shuffle reduction),
 //      LSE_i * log2(e), both padded per head to a multiple of 128 rows (+inf
 //      and 0 past N), and zero the fp32 dQ accumulator.
-//   2. dkdv: one CTA owns one 128-key tile of one kv head and loops over every
-//      query head of its group and every 128-query tile that can see it.  dK
-//      and dV accumulate in tensor memory and are written once: no atomics.
+//   2. dkdv: persistent, one CTA per SM; a unit is one 128-key tile of one kv
+//      head, and the CTA loops over every query head of its group and every
+//      128-query tile that can see it.  dK and dV accumulate in tensor memory
+//      and are written once per unit: no atomics.  The next unit's K / V load
+//      as soon as the unit's last MMAs are done.
 //      Per (query tile, key tile) it recomputes S^T = K Q^T, P^T = 2^(S^T *
 //      scale * log2 e - LSE * log2 e), dP^T = V dO^T, dS^T = P^T (dP^T - D),
 //      and issues dV += P^T dO, dK += dS^T Q, dQ_partial = dS K; the dQ
@@ -68,7 +70,7 @@ enum : int {
 };
 
 struct Bars {
-  uint64_t kv_full;
+  uint64_t kv_full, kv_empty, dkv_free;
   uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2], ld_full[2], ld_empty[2];
   uint64_t s_full, dp_full, p_full, dv_done, ds_full, dk_done, dq_full, dq_empty, dkv_done, drain;
   uint64_t st_full[2][2];   // [slot][group]: the group's dQ partial of the slot's item is staged
@@ -81,6 +83,34 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                    smem_u32(dst)),
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
+}
+
+// A unit is one 128-key tile of one kv head of one batch; its CTA loops over
+// every query head of the group and every query tile that sees the key tile
+// (causal: i >= j; window w: i <= (128j + 126 + w) / 128).  Units go
+// heaviest first (smallest key tile first), dealt to the persistent CTAs in
+// snake order: rounds alternate direction over the CTAs.
+struct Unit {
+  int kvh, b, j, i0, nqi, n_items;
+};
+
+__device__ __forceinline__ Unit decode_unit(int idx, const BwdArgs& a, int nt) {
+  const int per = a.Hkv * a.B;
+  Unit u;
+  u.j = idx / per;
+  const int kb = idx - u.j * per;
+  u.kvh = kb % a.Hkv;
+  u.b = kb / a.Hkv;
+  u.i0 = a.causal ? u.j : 0;
+  const int i1 = a.window > 0 ? min(nt, (u.j * kT + kT - 2 + a.window) / kT + 1) : nt;
+  u.nqi = i1 - u.i0;
+  u.n_items = (a.Hq / a.Hkv) * u.nqi;
+  return u;
+}
+
+__device__ __forceinline__ int unit_of_round(int k) {
+  const int g = gridDim.x;
+  return k * g + ((k & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x);
 }
 
 // kDq = false: dK and dV only (the deterministic backward computes dQ in its
@@ -109,21 +139,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kvh = blockIdx.x;
-  const int b = blockIdx.y;
-  const int j = blockIdx.z;                       // key tile (small j = most work, launched first)
   const int N = args.N;
   const int nt = (N + kT - 1) / kT;
   const int G = args.Hq / args.Hkv;
-  const int i0 = args.causal ? j : 0;            // first query tile that sees key tile j
-  // One past the last query tile that sees key tile j: with a window w the
-  // last query to see key 128j + 127 is 128j + 126 + w.
-  const int i1 = args.window > 0 ? min(nt, (j * kT + kT - 2 + args.window) / kT + 1) : nt;
-  const int nqi = i1 - i0;
-  const int n_items = G * nqi;
+  const int n_units = args.Hkv * args.B * nt;
+  // Items are counted across the CTA's units (T = items of earlier units), so
+  // the per-item barriers and the Q / dO / LSE slots run on without a break.
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);   // a unit's last MMAs done: K / V may be replaced
+    mbar_init(&bars->dkv_free, 256); // the unit's dK / dV read out of tensor memory
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], kDq ? 2 : 1);   // dK/dQ MMAs done (+ dQ staging read by TMA)
@@ -181,50 +207,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bars->kv_full, 2 * L::kTile);
-      for (int a = 0; a < kAtoms; ++a) {
-        tma_load_4d(smem + L::kK + a * kBlockBytes, &tmK, &bars->kv_full, a * 64, j * kT, kvh, b);
-        tma_load_4d(smem + L::kV + a * kBlockBytes, &tmV, &bars->kv_full, a * 64, j * kT, kvh, b);
-      }
       int n_ld[2] = {0, 0}, n_q[2] = {0, 0}, n_do[2] = {0, 0};   // copies issued per slot
-      // LSE*log2(e) and D of item u (512 bytes each) go to slot u % 2; they are
-      // issued one item ahead of that item's Q / dO tiles.
-      auto issue_ld = [&](int u) -> bool {
-        if (u >= n_items) return true;
-        const int slot = u & 1;
-        if (u >= 2 && !mbar_wait(&bars->ld_empty[slot], ((u >> 1) - 1) & 1, st, abort_flag, kSiteLdEmpty))
-          return false;
-        const int h = kvh * G + u / nqi;
-        const int i = i0 + u % nqi;
-        const size_t roff = ((size_t)b * args.Hq + h) * ntp + (size_t)i * kT;
-        mbar_arrive_expect_tx(&bars->ld_full[slot], 1024u);
-        bulk_load(smem + L::kLse + slot * 512, args.lse2 + roff, 512u, &bars->ld_full[slot]);
-        bulk_load(smem + L::kDr + slot * 512, args.drow + roff, 512u, &bars->ld_full[slot]);
-        ++n_ld[slot];
-        return true;
-      };
-      bool pok = issue_ld(0);
-      for (int t = 0; pok && t < n_items; ++t) {
-        const int h = kvh * G + t / nqi;
-        const int i = i0 + t % nqi;
-        const int slot = t & 1;
-        const uint32_t ph = ((t >> 1) - 1) & 1;   // phase of this slot's previous use
-        if (t >= 2 && !mbar_wait(&bars->q_empty[slot], ph, st, abort_flag, kSiteQEmpty)) break;
-        mbar_arrive_expect_tx(&bars->q_full[slot], L::kTile);
-        for (int a = 0; a < kAtoms; ++a)
-          tma_load_4d(smem + L::kQ + slot * L::kTile + a * kBlockBytes, &tmQ, &bars->q_full[slot], a * 64, i * kT,
-                      h, b);
-        ++n_q[slot];
-        if (t >= 2 && !mbar_wait(&bars->do_empty[slot], ph, st, abort_flag, kSiteDoEmpty)) break;
-        mbar_arrive_expect_tx(&bars->do_full[slot], L::kTile);
-        for (int a = 0; a < kAtoms; ++a)
-          tma_load_4d(smem + L::kDO + slot * L::kTile + a * kBlockBytes, &tmDO, &bars->do_full[slot], a * 64,
-                      i * kT, h, b);
-        ++n_do[slot];
-        pok = issue_ld(t + 1);
+      int n_kv = 0, T = 0;
+      bool pok = true;
+      for (int round = 0; pok; ++round) {
+        const int uidx = unit_of_round(round);
+        if (uidx >= n_units) break;
+        const Unit un = decode_unit(uidx, args, nt);
+        // LSE*log2(e) and D of local item u (512 bytes each) go to slot
+        // (T + u) % 2; they are issued one item ahead of that item's Q / dO.
+        auto issue_ld = [&](int u) -> bool {
+          if (u >= un.n_items) return true;
+          const int tg = T + u;
+          const int slot = tg & 1;
+          if (tg >= 2 && !mbar_wait(&bars->ld_empty[slot], ((tg >> 1) - 1) & 1, st, abort_flag, kSiteLdEmpty))
+            return false;
+          const int h = un.kvh * G + u / un.nqi;
+          const int i = un.i0 + u % un.nqi;
+          const size_t roff = ((size_t)un.b * args.Hq + h) * ntp + (size_t)i * kT;
+          mbar_arrive_expect_tx(&bars->ld_full[slot], 1024u);
+          bulk_load(smem + L::kLse + slot * 512, args.lse2 + roff, 512u, &bars->ld_full[slot]);
+          bulk_load(smem + L::kDr + slot * 512, args.drow + roff, 512u, &bars->ld_full[slot]);
+          ++n_ld[slot];
+          return true;
+        };
+        pok = issue_ld(0);
+        for (int t = 0; pok && t < un.n_items; ++t) {
+          const int tg = T + t;
+          const int h = un.kvh * G + t / un.nqi;
+          const int i = un.i0 + t % un.nqi;
+          const int slot = tg & 1;
+          const uint32_t ph = ((tg >> 1) - 1) & 1;   // phase of this slot's previous use
+          if (tg >= 2 && !mbar_wait(&bars->q_empty[slot], ph, st, abort_flag, kSiteQEmpty)) { pok = false; break; }
+          mbar_arrive_expect_tx(&bars->q_full[slot], L::kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_4d(smem + L::kQ + slot * L::kTile + a * kBlockBytes, &tmQ, &bars->q_full[slot], a * 64,
+                        i * kT, h, un.b);
+          ++n_q[slot];
+          if (tg >= 2 && !mbar_wait(&bars->do_empty[slot], ph, st, abort_flag, kSiteDoEmpty)) { pok = false; break; }
+          mbar_arrive_expect_tx(&bars->do_full[slot], L::kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_4d(smem + L::kDO + slot * L::kTile + a * kBlockBytes, &tmDO, &bars->do_full[slot], a * 64,
+                        i * kT, h, un.b);
+          ++n_do[slot];
+          if (t == 0) {
+            // K and V of the unit replace the previous unit's once its last
+            // MMAs have completed (the unit's first Q / dO are already on
+            // their way).
+            if (n_kv > 0 && !mbar_wait(&bars->kv_empty, (n_kv - 1) & 1, st, abort_flag, kSiteKV)) {
+              pok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bars->kv_full, 2 * L::kTile);
+            for (int a = 0; a < kAtoms; ++a) {
+              tma_load_4d(smem + L::kK + a * kBlockBytes, &tmK, &bars->kv_full, a * 64, un.j * kT, un.kvh, un.b);
+              tma_load_4d(smem + L::kV + a * kBlockBytes, &tmV, &bars->kv_full, a * 64, un.j * kT, un.kvh, un.b);
+            }
+            ++n_kv;
+          }
+          pok = issue_ld(t + 1);
+        }
+        T += un.n_items;
       }
       // Every copy issued must have landed before the CTA may exit.
-      mbar_wait_drain(&bars->kv_full, 0, st.timeout_ns);
+      if (n_kv) mbar_wait_drain(&bars->kv_full, (n_kv - 1) & 1, st.timeout_ns);
       for (int s = 0; s < 2; ++s) {
         if (n_ld[s]) mbar_wait_drain(&bars->ld_full[s], (n_ld[s] - 1) & 1, st.timeout_ns);
         if (n_q[s]) mbar_wait_drain(&bars->q_full[s], (n_q[s] - 1) & 1, st.timeout_ns);
@@ -237,32 +283,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);   // S^T, dP^T
       constexpr uint32_t idKM = idesc_bf16(128, D, false, true);      // dV, dK
       constexpr uint32_t idMM = idesc_bf16(128, D, true, true);       // dQ
-      bool ok = mbar_wait(&bars->kv_full, 0, st, abort_flag, kSiteKV);
-      for (int t = 0; ok && t < n_items; ++t) {
-        const int slot = t & 1;
-        const uint32_t sph = (t >> 1) & 1;   // slot phase
-        const uint32_t ph = t & 1;           // per-item barrier phase
-        const uint32_t pph = (t - 1) & 1;    // previous item's phase
+      bool ok = true;
+      int T = 0, nu = 0;
+      for (int round = 0; ok; ++round, ++nu) {
+        const int uidx = unit_of_round(round);
+        if (uidx >= n_units) break;
+        const Unit un = decode_unit(uidx, args, nt);
+        if (!mbar_wait(&bars->kv_full, nu & 1, st, abort_flag, kSiteKV)) break;
+      for (int t = 0; ok && t < un.n_items; ++t) {
+        const int tg = T + t;
+        const int slot = tg & 1;
+        const uint32_t sph = (tg >> 1) & 1;  // slot phase
+        const uint32_t ph = tg & 1;          // per-item barrier phase
+        const uint32_t pph = (tg - 1) & 1;   // previous item's phase
         const uint32_t qa = sQ + slot * L::kTile, da = sDO + slot * L::kTile;
-        if (!mbar_wait(&bars->q_full[slot], sph, st, abort_flag, kSiteQFull)) break;
+        if (!mbar_wait(&bars->q_full[slot], sph, st, abort_flag, kSiteQFull)) { ok = false; break; }
         // S_{t+1} overwrites the score region, which holds P^T_t (read by dV_t)
         // and dS^T_t (read by dK_t); dK_t is the later of the two.
-        if (t > 0 && !mbar_wait(&bars->dk_done, pph, st, abort_flag, kSiteDkDone)) break;
+        if (tg > 0 && !mbar_wait(&bars->dk_done, pph, st, abort_flag, kSiteDkDone)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
           mma_bf16_ss(tS, desc_kmajor(sK, k16, kBlockBytes), desc_kmajor(qa, k16, kBlockBytes), idSS, k16 > 0);
         mma_commit(&bars->s_full);
-        if (!mbar_wait(&bars->do_full[slot], sph, st, abort_flag, kSiteDoFull)) break;
+        if (!mbar_wait(&bars->do_full[slot], sph, st, abort_flag, kSiteDoFull)) { ok = false; break; }
         // dP_t overwrites the dQ partial of item t-1 (read out by then) or,
         // without dQ, dP^T of item t-1 (read before ds_full of t-1).
-        if (kDq && t > 0 && !mbar_wait(&bars->dq_empty, pph, st, abort_flag, kSiteDqEmpty)) break;
+        if (kDq && tg > 0 && !mbar_wait(&bars->dq_empty, pph, st, abort_flag, kSiteDqEmpty)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
           mma_bf16_ss(tDP, desc_kmajor(sV, k16, kBlockBytes), desc_kmajor(da, k16, kBlockBytes), idSS, k16 > 0);
         mma_commit(&bars->dp_full);
-        if (!mbar_wait(&bars->p_full, ph, st, abort_flag, kSitePFull)) break;
+        if (!mbar_wait(&bars->p_full, ph, st, abort_flag, kSitePFull)) { ok = false; break; }
+        // The unit's first dV / dK overwrite the previous unit's accumulators:
+        // its epilogue must have read them out.
+        if (t == 0 && nu > 0 && !mbar_wait(&bars->dkv_free, (nu - 1) & 1, st, abort_flag, kSiteDkvDone)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         // P^T for query columns 16*k16.. lives at column (k16/4)*64 + (k16%4)*8.
 #pragma unroll
@@ -271,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (t > 0 || k16 > 0) ? 1u : 0u);
         mma_commit(&bars->dv_done);
         mma_commit(&bars->do_empty[slot]);
-        if (!mbar_wait(&bars->ds_full, ph, st, abort_flag, kSiteDsFull)) break;
+        if (!mbar_wait(&bars->ds_full, ph, st, abort_flag, kSiteDsFull)) { ok = false; break; }
         tc_fence_after();
         // dS^T for query columns 16*k16.. lives at column (k16/4)*64 + 32 + (k16%4)*8.
 #pragma unroll
@@ -288,7 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&bars->q_empty[slot]);
       }
+      if (!ok) break;
       mma_commit(&bars->dkv_done);
+      mma_commit(&bars->kv_empty);
+      T += un.n_items;
+      }
       mma_commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, st.timeout_ns);
     }
@@ -298,19 +361,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const int key = j * kT + r;
     const int c0 = g * 64;                         // this group's query columns
     const float sl2 = args.scale_log2;
     const uint64_t sl2x2 = f2pack(sl2, sl2);
     bool ok = true;
-    for (int t = 0; t < n_items; ++t) {
-      const int slot = t & 1;
-      const uint32_t ph = t & 1;
-      const int i = i0 + t % nqi;
+    int T = 0, nu = 0;
+    for (int round = 0; ok; ++round, ++nu) {
+    const int uidx = unit_of_round(round);
+    if (uidx >= n_units) break;
+    const Unit un = decode_unit(uidx, args, nt);
+    const int key = un.j * kT + r;
+    for (int t = 0; t < un.n_items; ++t) {
+      const int tg = T + t;
+      const int slot = tg & 1;
+      const uint32_t ph = tg & 1;
+      const int i = un.i0 + t % un.nqi;
       auto dq_stage = [&](int q) { return stage_addr(slot, g, q); };
       const float* lse_t = reinterpret_cast<const float*>(smem + L::kLse + slot * 512) + c0;
       const float* dr_t = reinterpret_cast<const float*>(smem + L::kDr + slot * 512) + c0;
-      if (!mbar_wait_warp(&bars->ld_full[slot], (t >> 1) & 1, st, abort_flag, kSiteLdFull)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars->ld_full[slot], (tg >> 1) & 1, st, abort_flag, kSiteLdFull)) { ok = false; break; }
       if (!mbar_wait_warp(&bars->s_full, ph, st, abort_flag, kSiteSFull)) { ok = false; break; }
       tc_fence_after();
       uint32_t pr[2][32];
@@ -428,9 +497,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
-    if (ok && mbar_wait_warp(&bars->dkv_done, 0, st, abort_flag, kSiteDkvDone)) {
+    if (!ok || !mbar_wait_warp(&bars->dkv_done, nu & 1, st, abort_flag, kSiteDkvDone)) {
+      ok = false;
+      break;
+    }
+    {
       tc_fence_after();
-      const size_t kvrow = ((size_t)b * args.Hkv + kvh) * N + (size_t)key;
+      const size_t kvrow = ((size_t)un.b * args.Hkv + un.kvh) * N + (size_t)key;
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {
         const uint32_t src = (pass == 0 ? tDV : tDK) + lane_off + g * kHalfD;
@@ -442,6 +515,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(src + q * 32, v);
           tmem_wait_ld();
           reg_fence(v);
+          if (pass == 1 && q == kHalfD / 32 - 1) {
+            // Last read of the unit's accumulators: the next unit may start
+            // its first dV / dK MMA.
+            tc_fence_before();
+            mbar_arrive(&bars->dkv_free);
+          }
           if (key < N) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -456,6 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    T += un.n_items;
+    }
   } else {
     // ------------------------------------------------------------ dQ store
     // Per item: wait until both groups have staged their dQ partial, add each
@@ -464,12 +545,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Q slots back to the producer once TMA has read the staging.  Waiting
     // for those reads here keeps them off the compute warps.
     if (kDq && lane == 0) {
-      for (int t = 0; t < n_items; ++t) {
-        const int slot = t & 1;
-        const int head = b * args.Hq + kvh * G + t / nqi;
-        const int i = i0 + t % nqi;
-        if (!mbar_wait(&bars->st_full[slot][0], (t >> 1) & 1, st, abort_flag, kSiteStFull)) break;
-        if (!mbar_wait(&bars->st_full[slot][1], (t >> 1) & 1, st, abort_flag, kSiteStFull)) break;
+      bool sok = true;
+      int T = 0;
+      for (int round = 0; sok; ++round) {
+      const int uidx = unit_of_round(round);
+      if (uidx >= n_units) break;
+      const Unit un = decode_unit(uidx, args, nt);
+      for (int t = 0; t < un.n_items; ++t) {
+        const int tg = T + t;
+        const int slot = tg & 1;
+        const int head = un.b * args.Hq + un.kvh * G + t / un.nqi;
+        const int i = un.i0 + t % un.nqi;
+        if (!mbar_wait(&bars->st_full[slot][0], (tg >> 1) & 1, st, abort_flag, kSiteStFull) ||
+            !mbar_wait(&bars->st_full[slot][1], (tg >> 1) & 1, st, abort_flag, kSiteStFull)) {
+          sok = false;
+          break;
+        }
 #pragma unroll
         for (int in_q = 1; in_q >= 0; --in_q) {
 #pragma unroll
@@ -484,6 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->q_empty[slot]);
         bulk_wait_read<0>();
         mbar_arrive(&bars->do_empty[slot]);
+      }
+      T += un.n_items;
       }
       // The additions must have landed before the kernel is complete.
       bulk_wait_all();
@@ -566,28 +659,28 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float4* __
 template <int D, bool kDq>
 static cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, const DevStatus& st,
-                                 cudaStream_t stream) {
+                                 int num_sms, cudaStream_t stream) {
   using L = BwdSmem<D>;
   static_assert(L::kBytes <= 232448, "shared memory budget");
   static_assert(sizeof(Bars) <= 256, "barrier block");
   cudaError_t e =
       cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, kDq>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
-  const int nt = (a.N + kT - 1) / kT;
-  dim3 grid(a.Hkv, a.B, nt);
+  const long long units = (long long)a.Hkv * a.B * ((a.N + kT - 1) / kT);
+  const int grid = (int)(units < num_sms ? units : num_sms);
   fa_bwd_dkdv_kernel<D, kDq><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, a, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, const DevStatus& st,
-                            cudaStream_t stream) {
+                            int num_sms, cudaStream_t stream) {
   if (a.with_dq) {
-    if (d == 64) return launch_dkdv_d<64, true>(tq, tk, tv, tdo, tdq, a, st, stream);
-    return launch_dkdv_d<128, true>(tq, tk, tv, tdo, tdq, a, st, stream);
+    if (d == 64) return launch_dkdv_d<64, true>(tq, tk, tv, tdo, tdq, a, st, num_sms, stream);
+    return launch_dkdv_d<128, true>(tq, tk, tv, tdo, tdq, a, st, num_sms, stream);
   }
-  if (d == 64) return launch_dkdv_d<64, false>(tq, tk, tv, tdo, tdq, a, st, stream);
-  return launch_dkdv_d<128, false>(tq, tk, tv, tdo, tdq, a, st, stream);
+  if (d == 64) return launch_dkdv_d<64, false>(tq, tk, tv, tdo, tdq, a, st, num_sms, stream);
+  return launch_dkdv_d<128, false>(tq, tk, tv, tdo, tdq, a, st, num_sms, stream);
 }
 
 static int grid_for(long long work_items, int num_sms) {

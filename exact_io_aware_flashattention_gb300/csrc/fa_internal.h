@@ -65,7 +65,7 @@ cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dO, const fl
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, const DevStatus& st,
-                            cudaStream_t stream);
+                            int num_sms, cudaStream_t stream);
 
 cudaError_t launch_bwd_dq_convert(const float* dq_accum, void* dq, float scale, long long n, int num_sms,
                                   cudaStream_t stream);
