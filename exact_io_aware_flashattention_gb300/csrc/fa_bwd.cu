@@ -635,22 +635,42 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __r
   }
   if (dq_accum == nullptr) return;   // no accumulator (deterministic dQ)
   const long long n4 = heads * N * (D / 4);
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride)
-    dq_accum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += 4 * stride) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * stride < n4) dq_accum[i + u * stride] = z;
+  }
 }
 
 __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float4* __restrict__ acc,
                                                                 uint4* __restrict__ dq, float scale, long long n8) {
+  // Four independent 8-element groups per thread and iteration keep more
+  // loads in flight (the accumulator is mostly still in L2).
+  constexpr int kU = 4;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
-    const float4 a = acc[2 * i];
-    const float4 c = acc[2 * i + 1];
-    uint4 w;
-    w.x = cvt_bf16x2(a.x * scale, a.y * scale);
-    w.y = cvt_bf16x2(a.z * scale, a.w * scale);
-    w.z = cvt_bf16x2(c.x * scale, c.y * scale);
-    w.w = cvt_bf16x2(c.z * scale, c.w * scale);
-    dq[i] = w;
+  for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < n8; i0 += kU * stride) {
+    float4 a[kU], c[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const long long i = i0 + u * stride;
+      if (i < n8) {
+        a[u] = acc[2 * i];
+        c[u] = acc[2 * i + 1];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const long long i = i0 + u * stride;
+      if (i < n8) {
+        uint4 w;
+        w.x = cvt_bf16x2(a[u].x * scale, a[u].y * scale);
+        w.y = cvt_bf16x2(a[u].z * scale, a[u].w * scale);
+        w.z = cvt_bf16x2(c[u].x * scale, c[u].y * scale);
+        w.w = cvt_bf16x2(c[u].z * scale, c[u].w * scale);
+        dq[i] = w;
+      }
+    }
   }
 }
 
