@@ -142,3 +142,50 @@ def test_deterministic_backward_standard_workload(cuda_lib):
     fa.check_device_status()
     rdq, rdk, rdv = ref.attention_backward(f64(q), f64(k), f64(v), f64(do), True, w.scale)
     assert_bwd(dq, dk, dv, rdq, rdk, rdv, "deterministic standard causal workload")
+
+
+def test_more_splits_than_key_tiles(cuda_lib):
+    # num_splits larger than the number of key tiles: every split holds at
+    # least one tile (the chunk size is rounded up).
+    B, Hq, Hkv, Nq, Nk, d = 1, 4, 2, 3, 300, 64
+    q, k, v = gen(B, Hq, Hkv, Nq, Nk, d, seed=91)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    o, lse = fa.forward_ex(qd, kd, vd, causal=True, num_splits=100)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    ro, rl = ref.attention_forward(f64(q), f64(k), f64(v), True, d ** -0.5)
+    assert_fwd(o, lse, ro, rl, "100 splits over 3 key tiles")
+
+
+@pytest.mark.parametrize("N,window,splits", [(16, 0, 1), (16, 5, 1), (40, 0, 3), (130, 64, 2)])
+def test_self_attention_through_fwd_ex(cuda_lib, N, window, splits):
+    # Nq == Nk through the general entry point, with grouped heads small
+    # enough to be packed into one tile (N = 16, 40) or not (N = 130).
+    B, Hq, Hkv, d = 2, 8, 2, 128
+    q, k, v = gen(B, Hq, Hkv, N, N, d, seed=N + window)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    o, lse = fa.forward_ex(qd, kd, vd, causal=True, window=window, num_splits=splits)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    ro, rl = ref.attention_forward(f64(q), f64(k), f64(v), True, d ** -0.5, window=window)
+    assert_fwd(o, lse, ro, rl, f"N={N} window={window} splits={splits}")
+
+
+def test_decode_grouped_at_scale(cuda_lib):
+    # Grouped decode at the size of the grouped-query workload (32 query
+    # heads over 8 kv heads, 8192 keys), 4 new rows per head, default splits;
+    # the oracle checks two (batch, kv group) units drawn by seed.
+    B, Hq, Hkv, Nq, Nk, d = 2, 32, 8, 4, 8192, 128
+    q, k, v = gen(B, Hq, Hkv, Nq, Nk, d, seed=2024)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    o, lse = fa.forward_ex(qd, kd, vd, causal=True, num_splits=0)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    G = Hq // Hkv
+    rng = np.random.default_rng(7)
+    for u in rng.choice(B * Hkv, size=2, replace=False):
+        b, g = divmod(int(u), Hkv)
+        hs = slice(g * G, (g + 1) * G)
+        ro, rl = ref.attention_forward(f64(q[b:b + 1, hs]), f64(k[b:b + 1, g:g + 1]), f64(v[b:b + 1, g:g + 1]), True,
+                                       d ** -0.5)
+        assert_fwd(o[b:b + 1, hs], lse[b:b + 1, hs], ro, rl, f"decode unit (b={b}, kv={g})")
