@@ -72,7 +72,7 @@ enum : int {
 struct Bars {
   uint64_t kv_full, kv_empty, dkv_free;
   uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2], ld_full[2], ld_empty[2];
-  uint64_t s_full, dp_full, p_full, dv_done, ds_full, dk_done, dq_full, dq_empty, dkv_done, drain;
+  uint64_t s_full, dp_full, p_full, ds_full, dk_done, dq_full, dq_empty, dkv_done, drain;
   uint64_t st_full[2][2];   // [slot][group]: the group's dQ partial of the slot's item is staged
   uint32_t tmem_base;
   int abort;
@@ -162,7 +162,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_full, 256);
-    mbar_init(&bars->dv_done, 1);
     mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->dq_full, 1);
@@ -328,7 +327,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k16 = 0; k16 < kT / 16; ++k16)
           mma_bf16_ts(tDV, tS + (k16 >> 2) * 64 + (k16 & 3) * 8, desc_mnmajor(da, k16, kBlockBytes), idKM,
                       (t > 0 || k16 > 0) ? 1u : 0u);
-        mma_commit(&bars->dv_done);
         mma_commit(&bars->do_empty[slot]);
         if (!mbar_wait(&bars->ds_full, ph, st, abort_flag, kSiteDsFull)) { ok = false; break; }
         tc_fence_after();
