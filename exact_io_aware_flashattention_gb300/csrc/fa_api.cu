@@ -392,10 +392,11 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
 
   DeviceState* ds = nullptr;
   FA_TRY(device_state(&ds));
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   FA_TRY(tmap_rows_bf16(&tq, q, B, Hq, Nq, d));
   FA_TRY(tmap_bf16(&tk, k, B, Hkv, Nk, d));
   FA_TRY(tmap_bf16(&tv, v, B, Hkv, Nk, d));
+  FA_TRY(tmap_bf16(&to, o, B, Hq, Nq, d));
   fa::FwdArgs a;
   a.o = o;
   a.lse = lse;
@@ -415,7 +416,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
   a.split_tiles = g.split_tiles;
   a.scale_log2 = scale * 1.4426950408889634f;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  FA_TRY(launch_status(fa::launch_fwd(d, tq, tk, tv, a, dev_status(ds), ds->num_sms, st)));
+  FA_TRY(launch_status(fa::launch_fwd(d, tq, tk, tv, to, a, dev_status(ds), ds->num_sms, st)));
   if (g.splits > 1) FA_TRY(launch_status(fa::launch_fwd_merge(d, a, ds->num_sms, st)));
   return FA_OK;
 }

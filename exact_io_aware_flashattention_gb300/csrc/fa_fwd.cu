@@ -16,10 +16,11 @@
 // batch), heaviest causal tiles first, dealt to the CTAs in snake order.  CTA layout (384 threads):
 //   warp 0      TMA producer for Q (2 slots) and K (ring of kStagesK)
 //   warp 1      TMEM allocator; one thread issues the S = Q K^T MMAs
-//   warp 11     one thread issues the O += P V MMAs.  The two issuers touch
+//   warp 2      TMA producer for V (ring of kStagesV)
+//   warp 3      one thread issues the O += P V MMAs.  The two issuers touch
 //               disjoint tensor memory and each commit tracks only its own
 //               MMAs, so each waits only for what its MMAs need.
-//   warps 2-5   softmax group 0, warps 6-9 softmax group 1: the groups take
+//   warps 4-7   softmax group 0, warps 8-11 softmax group 1: the groups take
 //               alternate score tiles of the CTA's tile sequence (tile t goes
 //               to group t % 2); thread r of the owning group handles query
 //               row r (TMEM lane r), so row max and row sum are in-thread
@@ -29,7 +30,9 @@
 //               has its row max, then both groups' exponentials overlap.  Each
 //               group keeps its own part of the row sum; the two parts are
 //               combined in the item's epilogue.
-//   warp 10     TMA producer for V (ring of kStagesV)
+// The control warpgroup (warps 0-3) keeps kCtrlRegs registers a thread and
+// hands the rest of the launch allocation to the two softmax warpgroups,
+// which hold a 128-column score row in registers.
 // Tensor memory (512 columns): two fp32 128x128 score buffers at columns 0
 // and 128, two bf16 probability buffers (128 x 128 bf16 = 64 columns) at 256
 // and 320, and the O accumulator (fp32 128 x d) at 384.  Tile t uses score
@@ -51,6 +54,10 @@ constexpr int kBM = 128;        // query rows per tile
 constexpr int kBN = 128;        // keys per tile
 constexpr int kSBuf = 2;        // score buffers (and probability buffers) in tensor memory
 constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;                 // 65536 / 384, rounded down to the allocation unit of 8
+constexpr int kCtrlRegs = 56;
+constexpr int kSoftmaxRegs = (kLaunchRegs * 3 - kCtrlRegs) / 2;   // 224: the shares add up to the launch allocation
+static_assert(kSoftmaxRegs % 8 == 0 && kSoftmaxRegs <= 256, "register split");
 constexpr uint32_t kBlockBytes = 128u * 128u;   // one 64-column block of a 128-row bf16 tile
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -84,6 +91,7 @@ struct Bars {
   uint64_t hand[2];         // reference max of tile t published (by tile parity)
   uint64_t lx[2];           // row-sum part of the non-owner group published (by multi-tile item parity)
   uint64_t drain_s, drain_pv;
+  uint64_t stg_full[2];     // per softmax group: the O staging of its epilogue is written
   uint32_t tmem_base;
   int abort;
 };
@@ -196,7 +204,8 @@ struct Cursor {
 template <int D, bool kGeneral>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdArgs args, const DevStatus st) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const FwdArgs args,
+                  const DevStatus st) {
   using L = FwdCfg<D>;
   constexpr int kAtoms = D / 64;
   constexpr int SK = L::kStagesK, SV = L::kStagesV;
@@ -219,7 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1);
-      mbar_init(&bars->q_empty[i], 1);
+      // Last S of the item done (+ in the plain instance, the O epilogue's
+      // TMA store has read its staging, which reuses the item's Q slot).
+      mbar_init(&bars->q_empty[i], kGeneral ? 1 : 2);
       mbar_init(&bars->o_done[i], 1);
       mbar_init(&bars->hand[i], 128);
       mbar_init(&bars->lx[i], 128);
@@ -240,12 +251,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->o_free, 128);
     mbar_init(&bars->drain_s, 1);
     mbar_init(&bars->drain_pv, 1);
+    for (int x = 0; x < 2; ++x) mbar_init(&bars->stg_full[x], 128);
     bars->abort = 0;
     mbar_fence_init();
     fence_proxy_async_smem();
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    if (!kGeneral) tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -261,325 +274,379 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sK = smem_u32(smem + L::kK);
   const uint32_t sV = smem_u32(smem + L::kV);
 
-  if (warp == 0) {
-    // ------------------------------------------------------ Q / K producer
-    if (lane == 0) {
-      int kt = 0, li = 0;
-      int q_issued[2] = {0, 0};
-      bool ok = true;
-      for (int round = 0, item = item_of_round(0); ok && item < n_items; item = item_of_round(++round)) {
-        const Item it = decode_item<kGeneral>(item, args);
-        if (it.n == 0) continue;
-        const int slot = li & 1;
-        if (li >= 2 && !mbar_wait(&bars->q_empty[slot], ((li >> 1) - 1) & 1, st, abort_flag, kSiteQEmpty)) break;
-        mbar_arrive_expect_tx(&bars->q_full[slot], L::kTile);
-        for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(smem + L::kQ + slot * L::kTile + a * kBlockBytes, &tmQ, &bars->q_full[slot], a * 64,
-                      it.qrow, it.b);
-        ++q_issued[slot];
-        for (int j = 0; j < it.n; ++j, ++kt) {
-          const int s = kt % SK, r = kt / SK;
-          if (r > 0 && !mbar_wait(&bars->k_empty[s], (r - 1) & 1, st, abort_flag, kSiteKEmpty)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->k_full[s], L::kTile);
+  if (warp < 4) {
+    setmaxnreg_dec<kCtrlRegs>();
+    if (warp == 0) {
+      // ------------------------------------------------------ Q / K producer
+      if (lane == 0) {
+        int kt = 0, li = 0;
+        int q_issued[2] = {0, 0};
+        bool ok = true;
+        for (int round = 0, item = item_of_round(0); ok && item < n_items; item = item_of_round(++round)) {
+          const Item it = decode_item<kGeneral>(item, args);
+          if (it.n == 0) continue;
+          const int slot = li & 1;
+          if (li >= 2 && !mbar_wait(&bars->q_empty[slot], ((li >> 1) - 1) & 1, st, abort_flag, kSiteQEmpty)) break;
+          mbar_arrive_expect_tx(&bars->q_full[slot], L::kTile);
           for (int a = 0; a < kAtoms; ++a)
-            tma_load_4d(smem + L::kK + s * L::kTile + a * kBlockBytes, &tmK, &bars->k_full[s], a * 64,
-                        (it.j0 + j) * kBN, it.kvh, it.b);
+            tma_load_3d(smem + L::kQ + slot * L::kTile + a * kBlockBytes, &tmQ, &bars->q_full[slot], a * 64,
+                        it.qrow, it.b);
+          ++q_issued[slot];
+          for (int j = 0; j < it.n; ++j, ++kt) {
+            const int s = kt % SK, r = kt / SK;
+            if (r > 0 && !mbar_wait(&bars->k_empty[s], (r - 1) & 1, st, abort_flag, kSiteKEmpty)) { ok = false; break; }
+            mbar_arrive_expect_tx(&bars->k_full[s], L::kTile);
+            for (int a = 0; a < kAtoms; ++a)
+              tma_load_4d(smem + L::kK + s * L::kTile + a * kBlockBytes, &tmK, &bars->k_full[s], a * 64,
+                          (it.j0 + j) * kBN, it.kvh, it.b);
+          }
+          ++li;   // items with key tiles, in the order the MMA issuers' cursors count them
         }
-        ++li;   // items with key tiles, in the order the MMA issuers' cursors count them
-      }
-      // Every copy issued must have landed before the CTA may exit.
-      for (int i = 0; i < 2; ++i)
-        if (q_issued[i]) mbar_wait_drain(&bars->q_full[i], (q_issued[i] - 1) & 1, st.timeout_ns);
-      for (int s = 0; s < SK && s < kt; ++s) {
-        const int last = kt - 1 - ((kt - 1 - s) % SK);   // last tile issued into stage s
-        mbar_wait_drain(&bars->k_full[s], (last / SK) & 1, st.timeout_ns);
-      }
-    }
-  } else if (warp == 10) {
-    // ------------------------------------------------------ V producer
-    if (lane == 0) {
-      int vt = 0;
-      bool ok = true;
-      for (int round = 0, item = item_of_round(0); ok && item < n_items; item = item_of_round(++round)) {
-        const Item it = decode_item<kGeneral>(item, args);
-        for (int j = 0; j < it.n; ++j, ++vt) {
-          const int s = vt % SV, r = vt / SV;
-          if (r > 0 && !mbar_wait(&bars->v_empty[s], (r - 1) & 1, st, abort_flag, kSiteVEmpty)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->v_full[s], L::kTile);
-          for (int a = 0; a < kAtoms; ++a)
-            tma_load_4d(smem + L::kV + s * L::kTile + a * kBlockBytes, &tmV, &bars->v_full[s], a * 64,
-                        (it.j0 + j) * kBN, it.kvh, it.b);
+        // Every copy issued must have landed before the CTA may exit.
+        for (int i = 0; i < 2; ++i)
+          if (q_issued[i]) mbar_wait_drain(&bars->q_full[i], (q_issued[i] - 1) & 1, st.timeout_ns);
+        for (int s = 0; s < SK && s < kt; ++s) {
+          const int last = kt - 1 - ((kt - 1 - s) % SK);   // last tile issued into stage s
+          mbar_wait_drain(&bars->k_full[s], (last / SK) & 1, st.timeout_ns);
         }
       }
-      for (int s = 0; s < SV && s < vt; ++s) {
-        const int last = vt - 1 - ((vt - 1 - s) % SV);
-        mbar_wait_drain(&bars->v_full[s], (last / SV) & 1, st.timeout_ns);
+    } else if (warp == 2) {
+      // ------------------------------------------------------ V producer
+      if (lane == 0) {
+        int vt = 0;
+        bool ok = true;
+        for (int round = 0, item = item_of_round(0); ok && item < n_items; item = item_of_round(++round)) {
+          const Item it = decode_item<kGeneral>(item, args);
+          for (int j = 0; j < it.n; ++j, ++vt) {
+            const int s = vt % SV, r = vt / SV;
+            if (r > 0 && !mbar_wait(&bars->v_empty[s], (r - 1) & 1, st, abort_flag, kSiteVEmpty)) { ok = false; break; }
+            mbar_arrive_expect_tx(&bars->v_full[s], L::kTile);
+            for (int a = 0; a < kAtoms; ++a)
+              tma_load_4d(smem + L::kV + s * L::kTile + a * kBlockBytes, &tmV, &bars->v_full[s], a * 64,
+                          (it.j0 + j) * kBN, it.kvh, it.b);
+          }
+        }
+        for (int s = 0; s < SV && s < vt; ++s) {
+          const int last = vt - 1 - ((vt - 1 - s) % SV);
+          mbar_wait_drain(&bars->v_full[s], (last / SV) & 1, st.timeout_ns);
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------ S issuer
+      if (lane == 0) {
+        constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+        Cursor<kGeneral> sc;
+        sc.init(args, n_items);
+        for (int ts = 0; sc.valid; ++ts, sc.next(args)) {
+          const int buf = ts % kSBuf;
+          // S_ts reuses score buffer ts % 2 once the owner of tile ts-2 has read it.
+          if (ts >= 2 && !mbar_wait(&bars->s_free[buf], ((ts - 2) / kSBuf) & 1, st, abort_flag, kSiteSFree)) break;
+          if (sc.j == 0 &&
+              !mbar_wait(&bars->q_full[sc.li & 1], (sc.li >> 1) & 1, st, abort_flag, kSiteQFull))
+            break;
+          const int s = ts % SK;
+          if (!mbar_wait(&bars->k_full[s], (ts / SK) & 1, st, abort_flag, kSiteKFull)) break;
+          tc_fence_after();
+          const uint32_t qa = sQ + (sc.li & 1) * L::kTile;
+          const uint32_t ka = sK + s * L::kTile;
+  #pragma unroll
+          for (int k16 = 0; k16 < D / 16; ++k16)
+            mma_bf16_ss(tmem + buf * 128, desc_kmajor(qa, k16, kBlockBytes), desc_kmajor(ka, k16, kBlockBytes), idS,
+                        k16 > 0);
+          mma_commit(&bars->s_full[buf]);
+          mma_commit(&bars->k_empty[s]);
+          if (sc.j == sc.it.n - 1) mma_commit(&bars->q_empty[sc.li & 1]);
+        }
+        // No MMA may still be writing tensor memory when it is freed.
+        mma_commit(&bars->drain_s);
+        mbar_wait_drain(&bars->drain_s, 0, st.timeout_ns);
+      }
+    } else if (warp == 3) {
+      // ------------------------------------------------------ P V issuer
+      if (lane == 0) {
+        constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
+        Cursor<kGeneral> pc;
+        pc.init(args, n_items);
+        for (int t = 0; pc.valid; ++t, pc.next(args)) {
+          const int buf = t % kSBuf;
+          if (!mbar_wait(&bars->p_full[buf], (t / kSBuf) & 1, st, abort_flag, kSitePFull)) break;
+          const int v = t % SV;
+          if (!mbar_wait(&bars->v_full[v], (t / SV) & 1, st, abort_flag, kSiteVFull)) break;
+          if (pc.j == 0 && pc.li > 0 && !mbar_wait(&bars->o_free, (pc.li - 1) & 1, st, abort_flag, kSiteOFree)) break;
+          tc_fence_after();
+          const uint32_t va = sV + v * L::kTile;
+  #pragma unroll
+          for (int k16 = 0; k16 < kBN / 16; ++k16)
+            mma_bf16_ts(tO, tmem + 256 + buf * 64 + k16 * 8, desc_mnmajor(va, k16, kBlockBytes), idO,
+                        (pc.j > 0 || k16 > 0) ? 1u : 0u);
+          mma_commit(&bars->o_done[t & 1]);
+          mma_commit(&bars->v_empty[v]);
+        }
+        mma_commit(&bars->drain_pv);
+        mbar_wait_drain(&bars->drain_pv, 0, st.timeout_ns);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------ S issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
-      Cursor<kGeneral> sc;
-      sc.init(args, n_items);
-      for (int ts = 0; sc.valid; ++ts, sc.next(args)) {
-        const int buf = ts % kSBuf;
-        // S_ts reuses score buffer ts % 2 once the owner of tile ts-2 has read it.
-        if (ts >= 2 && !mbar_wait(&bars->s_free[buf], ((ts - 2) / kSBuf) & 1, st, abort_flag, kSiteSFree)) break;
-        if (sc.j == 0 &&
-            !mbar_wait(&bars->q_full[sc.li & 1], (sc.li >> 1) & 1, st, abort_flag, kSiteQFull))
-          break;
-        const int s = ts % SK;
-        if (!mbar_wait(&bars->k_full[s], (ts / SK) & 1, st, abort_flag, kSiteKFull)) break;
-        tc_fence_after();
-        const uint32_t qa = sQ + (sc.li & 1) * L::kTile;
-        const uint32_t ka = sK + s * L::kTile;
-#pragma unroll
-        for (int k16 = 0; k16 < D / 16; ++k16)
-          mma_bf16_ss(tmem + buf * 128, desc_kmajor(qa, k16, kBlockBytes), desc_kmajor(ka, k16, kBlockBytes), idS,
-                      k16 > 0);
-        mma_commit(&bars->s_full[buf]);
-        mma_commit(&bars->k_empty[s]);
-        if (sc.j == sc.it.n - 1) mma_commit(&bars->q_empty[sc.li & 1]);
-      }
-      // No MMA may still be writing tensor memory when it is freed.
-      mma_commit(&bars->drain_s);
-      mbar_wait_drain(&bars->drain_s, 0, st.timeout_ns);
-    }
-  } else if (warp == 11) {
-    // ------------------------------------------------------ P V issuer
-    if (lane == 0) {
-      constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
-      Cursor<kGeneral> pc;
-      pc.init(args, n_items);
-      for (int t = 0; pc.valid; ++t, pc.next(args)) {
+  } else {
+    setmaxnreg_inc<kSoftmaxRegs>();
+      // ------------------------------------------------------ softmax
+      const int g = (warp - 4) >> 2;               // softmax group 0 or 1: owns tiles t with t % 2 == g
+      const int quad = warp & 3;
+      const int r = quad * 32 + lane;              // row within the tile == TMEM lane
+      const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+      float* mref = reinterpret_cast<float*>(smem + L::kMref);   // [tile parity][row]
+      float* lxb = reinterpret_cast<float*>(smem + L::kLx);      // [item parity][row]
+      const float sl2 = args.scale_log2;
+      const uint64_t sl2x2 = f2pack(sl2, sl2);
+      float m_g = -INFINITY;                       // reference max this group's row sum is relative to
+      float l_g = 0.f;                             // this group's part of the row sum
+      int my_item = -1;                            // item the group's (l_g, m_g) belong to
+      int n_epi = 0;                               // item epilogues this group has done
+      int n_multi = 0;                             // items with >= 2 tiles completed so far
+      Cursor<kGeneral> c;
+      c.init(args, n_items);
+      for (int t = 0; c.valid; ++t, c.next(args)) {
+        const int j = c.j, n = c.it.n;
+        const int n_multi_before = n_multi;
+        const int multi_slot = n_multi & 1;
+        if (j == n - 1 && n >= 2) ++n_multi;
+        if ((t & 1) != g) continue;                // the other group's tile
         const int buf = t % kSBuf;
-        if (!mbar_wait(&bars->p_full[buf], (t / kSBuf) & 1, st, abort_flag, kSitePFull)) break;
-        const int v = t % SV;
-        if (!mbar_wait(&bars->v_full[v], (t / SV) & 1, st, abort_flag, kSiteVFull)) break;
-        if (pc.j == 0 && pc.li > 0 && !mbar_wait(&bars->o_free, (pc.li - 1) & 1, st, abort_flag, kSiteOFree)) break;
+        // Position of this thread's query among the keys.
+        const int qpos = kGeneral ? (args.packed ? r % args.Nq : c.it.qbase + r) + (Nk - args.Nq) : c.it.qbase + r;
+        const uint32_t tS = tmem + buf * 128 + lane_off;
+        if (!mbar_wait_warp(&bars->s_full[buf], (t / kSBuf) & 1, st, abort_flag, kSiteSFull)) break;
         tc_fence_after();
-        const uint32_t va = sV + v * L::kTile;
-#pragma unroll
-        for (int k16 = 0; k16 < kBN / 16; ++k16)
-          mma_bf16_ts(tO, tmem + 256 + buf * 64 + k16 * 8, desc_mnmajor(va, k16, kBlockBytes), idO,
-                      (pc.j > 0 || k16 > 0) ? 1u : 0u);
-        mma_commit(&bars->o_done[t & 1]);
-        mma_commit(&bars->v_empty[v]);
-      }
-      mma_commit(&bars->drain_pv);
-      mbar_wait_drain(&bars->drain_pv, 0, st.timeout_ns);
-    }
-  } else if (warp >= 2 && warp <= 9) {
-    // ------------------------------------------------------ softmax
-    const int g = (warp - 2) >> 2;               // softmax group 0 or 1: owns tiles t with t % 2 == g
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;              // row within the tile == TMEM lane
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    float* mref = reinterpret_cast<float*>(smem + L::kMref);   // [tile parity][row]
-    float* lxb = reinterpret_cast<float*>(smem + L::kLx);      // [item parity][row]
-    const float sl2 = args.scale_log2;
-    const uint64_t sl2x2 = f2pack(sl2, sl2);
-    float m_g = -INFINITY;                       // reference max this group's row sum is relative to
-    float l_g = 0.f;                             // this group's part of the row sum
-    int my_item = -1;                            // item the group's (l_g, m_g) belong to
-    int n_multi = 0;                             // items with >= 2 tiles completed so far
-    Cursor<kGeneral> c;
-    c.init(args, n_items);
-    for (int t = 0; c.valid; ++t, c.next(args)) {
-      const int j = c.j, n = c.it.n;
-      const int n_multi_before = n_multi;
-      const int multi_slot = n_multi & 1;
-      if (j == n - 1 && n >= 2) ++n_multi;
-      if ((t & 1) != g) continue;                // the other group's tile
-      const int buf = t % kSBuf;
-      // Position of this thread's query among the keys.
-      const int qpos = kGeneral ? (args.packed ? r % args.Nq : c.it.qbase + r) + (Nk - args.Nq) : c.it.qbase + r;
-      const uint32_t tS = tmem + buf * 128 + lane_off;
-      if (!mbar_wait_warp(&bars->s_full[buf], (t / kSBuf) & 1, st, abort_flag, kSiteSFull)) break;
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int q = 0; q < 4; ++q) reg_fence(sr[q]);
-      tc_fence_before();
-      mbar_arrive(&bars->s_free[buf]);   // the MMA may compute S_{t+2} into this buffer now
-
-      const int key0 = (c.it.j0 + j) * kBN;
-      const bool windowed = kGeneral && args.window > 0;
-      if ((key0 + kBN > Nk) || (args.causal && key0 + kBN - 1 > c.it.qmin) ||
-          (windowed && key0 < c.it.qmax - args.window + 1)) {
-        // Keys [key0 + lo, key0 + hi) are visible to this row.
-        const int hi = min(Nk, args.causal ? qpos + 1 : Nk) - key0;
-        const int lo = windowed ? qpos - args.window + 1 - key0 : 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (q * 32 + e >= hi || q * 32 + e < lo) sr[q][e] = __float_as_uint(-INFINITY);
-      }
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          mx0 = fmax3(mx0, __uint_as_float(sr[q][e + 0]), __uint_as_float(sr[q][e + 1]));
-          mx1 = fmax3(mx1, __uint_as_float(sr[q][e + 2]), __uint_as_float(sr[q][e + 3]));
-          mx2 = fmax3(mx2, __uint_as_float(sr[q][e + 4]), __uint_as_float(sr[q][e + 5]));
-          mx3 = fmax3(mx3, __uint_as_float(sr[q][e + 6]), __uint_as_float(sr[q][e + 7]));
-        }
-      }
-      const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-      // Reference max after the previous tile (owned by the other group).  The
-      // wait also happens at an item's first tile, where the value is unused:
-      // it keeps the two groups' hand-offs strictly alternating, so no hand
-      // barrier can run two phases ahead of its waiter.
-      float m_prev = -INFINITY;
-      if (t > 0) {
-        if (!mbar_wait_warp(&bars->hand[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteHand)) break;
-        if (j > 0) m_prev = mref[((t - 1) & 1) * 128 + r];
-      }
-      const bool need = (j == 0) || (m_cand > m_prev + kRescaleThreshold);
-      const float m_new = need ? m_cand : m_prev;
-      // Hand the reference on to the owner of tile t+1 right away.
-      mref[(t & 1) * 128 + r] = m_new;
-      mbar_arrive(&bars->hand[t & 1]);
-
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      if (my_item != c.item) {
-        my_item = c.item;
-        l_g = 0.f;
-      } else if (m_g != m_new) {
-        l_g *= ex2(m_g - m_use);
-      }
-      m_g = m_new;
-
-      // P = 2^(s*sl2 - m), 32 keys at a time, into probability buffer t % 2
-      // once P V_{t-2} has consumed it.
-      if (t >= 2 && !mbar_wait_warp(&bars->o_done[t & 1], ((t >> 1) - 1) & 1, st, abort_flag, kSitePPrev)) break;
-      tc_fence_after();
-      const uint32_t tP = tmem + 256 + buf * 64 + lane_off;
-      const uint64_t negm = f2pack(-m_use, -m_use);
-      uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          uint64_t x[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint64_t sv = f2pack(__uint_as_float(sr[q][e + 2 * u]), __uint_as_float(sr[q][e + 2 * u + 1]));
-            float lo, hi;
-            f2unpack(ffma2(sv, sl2x2, negm), lo, hi);
-            lo = ex2(lo);
-            hi = ex2(hi);
-            x[u] = f2pack(lo, hi);
-            pk[e / 2 + u] = cvt_bf16x2(lo, hi);
-          }
-          acc0 = fadd2(acc0, x[0]);
-          acc1 = fadd2(acc1, x[1]);
-          acc2 = fadd2(acc2, x[2]);
-          acc3 = fadd2(acc3, x[3]);
-        }
-        tmem_st16(tP + q * 16, pk);
-      }
-      float a0, a1;
-      f2unpack(fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3)), a0, a1);
-      l_g += a0 + a1;
-
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O holds rows relative to the previous reference: rescale it once
-        // P V of the previous tile has landed.
-        const float alpha = need ? ex2(m_prev - m_use) : 1.f;
-        if (!mbar_wait_warp(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteORescale)) break;
-        tc_fence_after();
-        const uint64_t al2 = f2pack(alpha, alpha);
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t o[32];
-          tmem_ld32(tO + lane_off + q * 32, o);
-          tmem_wait_ld();
-          reg_fence(o);
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float lo, hi;
-            f2unpack(fmul2(f2pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), al2), lo, hi);
-            o[e] = __float_as_uint(lo);
-            o[e + 1] = __float_as_uint(hi);
-          }
-          tmem_st32(tO + lane_off + q * 32, o);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[buf]);
-
-      if (j == n - 2) {
-        // The other group owns the item's last tile: hand it this group's
-        // row-sum part, relative to m_new (which it reads back as m_prev).
-        lxb[multi_slot * 128 + r] = l_g;
-        mbar_arrive(&bars->lx[multi_slot]);
-      }
-      if (j == n - 1) {
-        // ------------------------------------------------ epilogue of the item
-        float l_tot = l_g;
-        if (n >= 2) {
-          if (!mbar_wait_warp(&bars->lx[multi_slot], (n_multi_before >> 1) & 1, st, abort_flag, kSiteLx)) break;
-          l_tot += lxb[multi_slot * 128 + r] * ex2(m_prev - m_use);
-        }
-        if (!mbar_wait_warp(&bars->o_done[t & 1], (t >> 1) & 1, st, abort_flag, kSiteOLast)) break;
-        tc_fence_after();
-        uint32_t o[D / 32][32];
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) tmem_ld32(tO + lane_off + q * 32, o[q]);
+        uint32_t sr[4][32];
+  #pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
         tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) reg_fence(o[q]);
+  #pragma unroll
+        for (int q = 0; q < 4; ++q) reg_fence(sr[q]);
         tc_fence_before();
-        mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
-        const long long frow = c.it.row0 + r;
-        if (r < c.it.rows) {
-          if (!kGeneral || args.splits == 1) {
+        mbar_arrive(&bars->s_free[buf]);   // the MMA may compute S_{t+2} into this buffer now
+
+        const int key0 = (c.it.j0 + j) * kBN;
+        const bool windowed = kGeneral && args.window > 0;
+        if ((key0 + kBN > Nk) || (args.causal && key0 + kBN - 1 > c.it.qmin) ||
+            (windowed && key0 < c.it.qmax - args.window + 1)) {
+          // Keys [key0 + lo, key0 + hi) are visible to this row.
+          const int hi = min(Nk, args.causal ? qpos + 1 : Nk) - key0;
+          const int lo = windowed ? qpos - args.window + 1 - key0 : 0;
+  #pragma unroll
+          for (int q = 0; q < 4; ++q)
+  #pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (q * 32 + e >= hi || q * 32 + e < lo) sr[q][e] = __float_as_uint(-INFINITY);
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+  #pragma unroll
+        for (int q = 0; q < 4; ++q) {
+  #pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            mx0 = fmax3(mx0, __uint_as_float(sr[q][e + 0]), __uint_as_float(sr[q][e + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(sr[q][e + 2]), __uint_as_float(sr[q][e + 3]));
+            mx2 = fmax3(mx2, __uint_as_float(sr[q][e + 4]), __uint_as_float(sr[q][e + 5]));
+            mx3 = fmax3(mx3, __uint_as_float(sr[q][e + 6]), __uint_as_float(sr[q][e + 7]));
+          }
+        }
+        const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        // Reference max after the previous tile (owned by the other group).  The
+        // wait also happens at an item's first tile, where the value is unused:
+        // it keeps the two groups' hand-offs strictly alternating, so no hand
+        // barrier can run two phases ahead of its waiter.
+        float m_prev = -INFINITY;
+        if (t > 0) {
+          if (!mbar_wait_warp(&bars->hand[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteHand)) break;
+          if (j > 0) m_prev = mref[((t - 1) & 1) * 128 + r];
+        }
+        const bool need = (j == 0) || (m_cand > m_prev + kRescaleThreshold);
+        const float m_new = need ? m_cand : m_prev;
+        // Hand the reference on to the owner of tile t+1 right away.
+        mref[(t & 1) * 128 + r] = m_new;
+        mbar_arrive(&bars->hand[t & 1]);
+
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        if (my_item != c.item) {
+          my_item = c.item;
+          l_g = 0.f;
+        } else if (m_g != m_new) {
+          l_g *= ex2(m_g - m_use);
+        }
+        m_g = m_new;
+
+        // P = 2^(s*sl2 - m), 32 keys at a time, into probability buffer t % 2
+        // once P V_{t-2} has consumed it.
+        if (t >= 2 && !mbar_wait_warp(&bars->o_done[t & 1], ((t >> 1) - 1) & 1, st, abort_flag, kSitePPrev)) break;
+        tc_fence_after();
+        const uint32_t tP = tmem + 256 + buf * 64 + lane_off;
+        const uint64_t negm = f2pack(-m_use, -m_use);
+        uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
+  #pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pk[16];
+  #pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint64_t x[4];
+  #pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint64_t sv = f2pack(__uint_as_float(sr[q][e + 2 * u]), __uint_as_float(sr[q][e + 2 * u + 1]));
+              float lo, hi;
+              f2unpack(ffma2(sv, sl2x2, negm), lo, hi);
+              lo = ex2(lo);
+              hi = ex2(hi);
+              x[u] = f2pack(lo, hi);
+              pk[e / 2 + u] = cvt_bf16x2(lo, hi);
+            }
+            acc0 = fadd2(acc0, x[0]);
+            acc1 = fadd2(acc1, x[1]);
+            acc2 = fadd2(acc2, x[2]);
+            acc3 = fadd2(acc3, x[3]);
+          }
+          tmem_st16(tP + q * 16, pk);
+        }
+        float a0, a1;
+        f2unpack(fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3)), a0, a1);
+        l_g += a0 + a1;
+
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // O holds rows relative to the previous reference: rescale it once
+          // P V of the previous tile has landed.
+          const float alpha = need ? ex2(m_prev - m_use) : 1.f;
+          if (!mbar_wait_warp(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteORescale)) break;
+          tc_fence_after();
+          const uint64_t al2 = f2pack(alpha, alpha);
+  #pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32(tO + lane_off + q * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+  #pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float lo, hi;
+              f2unpack(fmul2(f2pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), al2), lo, hi);
+              o[e] = __float_as_uint(lo);
+              o[e + 1] = __float_as_uint(hi);
+            }
+            tmem_st32(tO + lane_off + q * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[buf]);
+
+        if (j == n - 2) {
+          // The other group owns the item's last tile: hand it this group's
+          // row-sum part, relative to m_new (which it reads back as m_prev).
+          lxb[multi_slot * 128 + r] = l_g;
+          mbar_arrive(&bars->lx[multi_slot]);
+        }
+        if (j == n - 1) {
+          // ------------------------------------------------ epilogue of the item
+          float l_tot = l_g;
+          if (n >= 2) {
+            if (!mbar_wait_warp(&bars->lx[multi_slot], (n_multi_before >> 1) & 1, st, abort_flag, kSiteLx)) break;
+            l_tot += lxb[multi_slot * 128 + r] * ex2(m_prev - m_use);
+          }
+          if (!mbar_wait_warp(&bars->o_done[t & 1], (t >> 1) & 1, st, abort_flag, kSiteOLast)) break;
+          tc_fence_after();
+          const long long frow = c.it.row0 + r;
+          if (!kGeneral) {
+            // Plain instance: every thread writes its O row, normalised to
+            // bf16, into the item's Q slot (free: the item's last S has
+            // completed), 128-byte swizzled like the tensor map's box, 64
+            // columns at a time; one thread then writes the tile with TMA
+            // stores (rows past N are clipped) -- far cheaper for the group
+            // than 128 threads storing one row each.
             const float inv_l = 1.f / l_tot;
-            __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.o) + frow * D;
-#pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-#pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                uint4 w;
-                w.x = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 0]) * inv_l, __uint_as_float(o[q][v * 8 + 1]) * inv_l);
-                w.y = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 2]) * inv_l, __uint_as_float(o[q][v * 8 + 3]) * inv_l);
-                w.z = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 4]) * inv_l, __uint_as_float(o[q][v * 8 + 5]) * inv_l);
-                w.w = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 6]) * inv_l, __uint_as_float(o[q][v * 8 + 7]) * inv_l);
-                *reinterpret_cast<uint4*>(orow + q * 32 + v * 8) = w;
+            const uint32_t stage = smem_u32(smem + L::kQ) + (c.li & 1) * L::kTile;
+  #pragma unroll
+            for (int a = 0; a < kAtoms; ++a) {
+              uint32_t o[2][32];
+              tmem_ld32(tO + lane_off + a * 64, o[0]);
+              tmem_ld32(tO + lane_off + a * 64 + 32, o[1]);
+              tmem_wait_ld();
+              reg_fence(o[0]);
+              reg_fence(o[1]);
+  #pragma unroll
+              for (int q = 0; q < 2; ++q) {
+  #pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  const uint32_t w0 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 0]) * inv_l, __uint_as_float(o[q][v * 8 + 1]) * inv_l);
+                  const uint32_t w1 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 2]) * inv_l, __uint_as_float(o[q][v * 8 + 3]) * inv_l);
+                  const uint32_t w2 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 4]) * inv_l, __uint_as_float(o[q][v * 8 + 5]) * inv_l);
+                  const uint32_t w3 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 6]) * inv_l, __uint_as_float(o[q][v * 8 + 7]) * inv_l);
+                  // Columns a*64 + q*32 + v*8 .. +7: block a, 16-byte chunk q*4 + v.
+                  st_shared_v4(stage + a * kBlockBytes + swz128(r, q * 4 + v), w0, w1, w2, w3);
+                }
               }
             }
-            args.lse[frow] = (m_new + __log2f(l_tot)) * 0.69314718055994530942f;
-          } else {
-            // One key split: O normalised within the split, fp32, and its LSE;
-            // a row that sees no key of the split gets O = 0, LSE = -inf.
-            const long long prow = (long long)c.it.split * args.B * args.Hq * args.Nq + frow;
-            const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-            float4* orow = reinterpret_cast<float4*>(args.o_part + prow * D);
-#pragma unroll
-            for (int q = 0; q < D / 32; ++q)
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                orow[q * 8 + v] = make_float4(__uint_as_float(o[q][v * 4 + 0]) * inv_l,
-                                              __uint_as_float(o[q][v * 4 + 1]) * inv_l,
-                                              __uint_as_float(o[q][v * 4 + 2]) * inv_l,
-                                              __uint_as_float(o[q][v * 4 + 3]) * inv_l);
-            args.lse_part[prow] =
-                l_tot > 0.f ? (m_new + __log2f(l_tot)) * 0.69314718055994530942f : -INFINITY;
+            tc_fence_before();
+            mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
+            if (r < c.it.rows) args.lse[frow] = (m_new + __log2f(l_tot)) * 0.69314718055994530942f;
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->stg_full[g]);
+            if (quad == 0 && lane == 0) {
+              if (!mbar_wait(&bars->stg_full[g], n_epi & 1, st, abort_flag, kSiteOLast)) break;
+  #pragma unroll
+              for (int a = 0; a < kAtoms; ++a)
+                tma_store_4d(&tmO, stage + a * kBlockBytes, a * 64, c.it.qbase, c.it.h, c.it.b);
+              bulk_commit_group();
+              bulk_wait_read<0>();   // the Q slot may be reloaded once TMA has read the staging
+              mbar_arrive(&bars->q_empty[c.li & 1]);
+            }
+            ++n_epi;
+            continue;
+          }
+          uint32_t o[D / 32][32];
+  #pragma unroll
+          for (int q = 0; q < D / 32; ++q) tmem_ld32(tO + lane_off + q * 32, o[q]);
+          tmem_wait_ld();
+  #pragma unroll
+          for (int q = 0; q < D / 32; ++q) reg_fence(o[q]);
+          tc_fence_before();
+          mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
+          if (r < c.it.rows) {
+            if (args.splits == 1) {
+              const float inv_l = 1.f / l_tot;
+              __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.o) + frow * D;
+  #pragma unroll
+              for (int q = 0; q < D / 32; ++q) {
+  #pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  uint4 w;
+                  w.x = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 0]) * inv_l, __uint_as_float(o[q][v * 8 + 1]) * inv_l);
+                  w.y = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 2]) * inv_l, __uint_as_float(o[q][v * 8 + 3]) * inv_l);
+                  w.z = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 4]) * inv_l, __uint_as_float(o[q][v * 8 + 5]) * inv_l);
+                  w.w = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 6]) * inv_l, __uint_as_float(o[q][v * 8 + 7]) * inv_l);
+                  *reinterpret_cast<uint4*>(orow + q * 32 + v * 8) = w;
+                }
+              }
+              args.lse[frow] = (m_new + __log2f(l_tot)) * 0.69314718055994530942f;
+            } else {
+              // One key split: O normalised within the split, fp32, and its LSE;
+              // a row that sees no key of the split gets O = 0, LSE = -inf.
+              const long long prow = (long long)c.it.split * args.B * args.Hq * args.Nq + frow;
+              const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+              float4* orow = reinterpret_cast<float4*>(args.o_part + prow * D);
+  #pragma unroll
+              for (int q = 0; q < D / 32; ++q)
+  #pragma unroll
+                for (int v = 0; v < 8; ++v)
+                  orow[q * 8 + v] = make_float4(__uint_as_float(o[q][v * 4 + 0]) * inv_l,
+                                                __uint_as_float(o[q][v * 4 + 1]) * inv_l,
+                                                __uint_as_float(o[q][v * 4 + 2]) * inv_l,
+                                                __uint_as_float(o[q][v * 4 + 3]) * inv_l);
+              args.lse_part[prow] =
+                  l_tot > 0.f ? (m_new + __log2f(l_tot)) * 0.69314718055994530942f : -INFINITY;
+            }
           }
         }
       }
-    }
   }
 
+  // TMA stores of the O epilogue must be complete before the CTA exits.
+  if (!kGeneral) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -593,27 +660,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool kGeneral>
 static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const FwdArgs& a, const DevStatus& st, int num_sms, cudaStream_t stream) {
+                                const CUtensorMap& to, const FwdArgs& a, const DevStatus& st, int num_sms,
+                                cudaStream_t stream) {
   using L = FwdCfg<D>;
   static_assert(L::kBytes <= 232448, "shared memory budget");
   static_assert(sizeof(Bars) <= 512, "barrier block");
   cudaError_t e =
       cudaFuncSetAttribute(fa_fwd_kernel<D, kGeneral>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
+  // The warpgroups' register shares assume this launch allocation; with any
+  // other, the softmax warpgroups' increase could never be granted.
+  cudaFuncAttributes fattr;
+  e = cudaFuncGetAttributes(&fattr, fa_fwd_kernel<D, kGeneral>);
+  if (e != cudaSuccess) return e;
+  if (fattr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   const long long items = (long long)a.nqt * a.splits * a.units;
   const int grid = (int)(items < num_sms ? items : num_sms);
-  fa_fwd_kernel<D, kGeneral><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, a, st);
+  fa_fwd_kernel<D, kGeneral><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, to, a, st);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
-                       const DevStatus& st, int num_sms, cudaStream_t stream) {
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& to, const FwdArgs& a, const DevStatus& st, int num_sms,
+                       cudaStream_t stream) {
   const bool general = a.Nq != a.Nk || a.window > 0 || a.splits > 1 || a.packed;
   if (d == 64)
-    return general ? launch_fwd_d<64, true>(tq, tk, tv, a, st, num_sms, stream)
-                   : launch_fwd_d<64, false>(tq, tk, tv, a, st, num_sms, stream);
-  return general ? launch_fwd_d<128, true>(tq, tk, tv, a, st, num_sms, stream)
-                 : launch_fwd_d<128, false>(tq, tk, tv, a, st, num_sms, stream);
+    return general ? launch_fwd_d<64, true>(tq, tk, tv, to, a, st, num_sms, stream)
+                   : launch_fwd_d<64, false>(tq, tk, tv, to, a, st, num_sms, stream);
+  return general ? launch_fwd_d<128, true>(tq, tk, tv, to, a, st, num_sms, stream)
+                 : launch_fwd_d<128, false>(tq, tk, tv, to, a, st, num_sms, stream);
 }
 
 // Merge of the key splits ([Lecture] "推导 FlashAttention 的在线 softmax": both

@@ -54,8 +54,11 @@ struct DqArgs {
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, cudaStream_t stream);
 
-cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
-                       const DevStatus& st, int num_sms, cudaStream_t stream);
+// `to` (O as a {d, N, Hq, B} bf16 map) is used by the plain self-attention
+// instance only.
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& to, const FwdArgs& a, const DevStatus& st, int num_sms,
+                       cudaStream_t stream);
 
 // (O, LSE) of several key splits -> O (bf16), LSE.
 cudaError_t launch_fwd_merge(int d, const FwdArgs& a, int num_sms, cudaStream_t stream);

@@ -181,6 +181,14 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t
       : "memory");
 }
 
+// Tiled 4-D store of a shared-memory box to global memory, tracked by this
+// thread's bulk group (rows outside the tensor are not written).
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, uint32_t ssrc, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(ssrc)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most kPending of this thread's most recent bulk groups are
 // still reading shared memory.
@@ -199,6 +207,18 @@ __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
                "r"(ncols)
                : "memory");
+}
+// Per-thread register budget of the executing warpgroup (all four warps of
+// the warpgroup must execute the same instruction).  An increase waits until
+// the registers released by other warpgroups of the CTA cover it, so the
+// shares must add up to the launch allocation.
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 __device__ __forceinline__ void tmem_relinquish() {
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
