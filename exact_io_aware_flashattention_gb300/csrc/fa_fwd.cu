@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t qa = sQ + (sc.li & 1) * L::kTile;
           const uint32_t ka = sK + s * L::kTile;
-  #pragma unroll
+#pragma unroll
           for (int k16 = 0; k16 < D / 16; ++k16)
             mma_bf16_ss(tmem + buf * 128, desc_kmajor(qa, k16, kBlockBytes), desc_kmajor(ka, k16, kBlockBytes), idS,
                         k16 > 0);
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (pc.j == 0 && pc.li > 0 && !mbar_wait(&bars->o_free, (pc.li - 1) & 1, st, abort_flag, kSiteOFree)) break;
           tc_fence_after();
           const uint32_t va = sV + v * L::kTile;
-  #pragma unroll
+#pragma unroll
           for (int k16 = 0; k16 < kBN / 16; ++k16)
             mma_bf16_ts(tO, tmem + 256 + buf * 64 + k16 * 8, desc_mnmajor(va, k16, kBlockBytes), idO,
                         (pc.j > 0 || k16 > 0) ? 1u : 0u);
@@ -388,221 +388,220 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     setmaxnreg_inc<kSoftmaxRegs>();
-      // ------------------------------------------------------ softmax
-      const int g = (warp - 4) >> 2;               // softmax group 0 or 1: owns tiles t with t % 2 == g
-      const int quad = warp & 3;
-      const int r = quad * 32 + lane;              // row within the tile == TMEM lane
-      const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-      float* mref = reinterpret_cast<float*>(smem + L::kMref);   // [tile parity][row]
-      float* lxb = reinterpret_cast<float*>(smem + L::kLx);      // [item parity][row]
-      const float sl2 = args.scale_log2;
-      const uint64_t sl2x2 = f2pack(sl2, sl2);
-      float m_g = -INFINITY;                       // reference max this group's row sum is relative to
-      float l_g = 0.f;                             // this group's part of the row sum
-      int my_item = -1;                            // item the group's (l_g, m_g) belong to
-      int n_epi = 0;                               // item epilogues this group has done
-      int n_multi = 0;                             // items with >= 2 tiles completed so far
-      Cursor<kGeneral> c;
-      c.init(args, n_items);
-      for (int t = 0; c.valid; ++t, c.next(args)) {
-        const int j = c.j, n = c.it.n;
-        const int n_multi_before = n_multi;
-        const int multi_slot = n_multi & 1;
-        if (j == n - 1 && n >= 2) ++n_multi;
-        if ((t & 1) != g) continue;                // the other group's tile
-        const int buf = t % kSBuf;
-        // Position of this thread's query among the keys.
-        const int qpos = kGeneral ? (args.packed ? r % args.Nq : c.it.qbase + r) + (Nk - args.Nq) : c.it.qbase + r;
-        const uint32_t tS = tmem + buf * 128 + lane_off;
-        if (!mbar_wait_warp(&bars->s_full[buf], (t / kSBuf) & 1, st, abort_flag, kSiteSFull)) break;
-        tc_fence_after();
-        uint32_t sr[4][32];
-  #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
-        tmem_wait_ld();
-  #pragma unroll
-        for (int q = 0; q < 4; ++q) reg_fence(sr[q]);
-        tc_fence_before();
-        mbar_arrive(&bars->s_free[buf]);   // the MMA may compute S_{t+2} into this buffer now
+    // ------------------------------------------------------ softmax
+    const int g = (warp - 4) >> 2;               // softmax group 0 or 1: owns tiles t with t % 2 == g
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;              // row within the tile == TMEM lane
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    float* mref = reinterpret_cast<float*>(smem + L::kMref);   // [tile parity][row]
+    float* lxb = reinterpret_cast<float*>(smem + L::kLx);      // [item parity][row]
+    const float sl2 = args.scale_log2;
+    const uint64_t sl2x2 = f2pack(sl2, sl2);
+    float m_g = -INFINITY;                       // reference max this group's row sum is relative to
+    float l_g = 0.f;                             // this group's part of the row sum
+    int my_item = -1;                            // item the group's (l_g, m_g) belong to
+    int n_epi = 0;                               // item epilogues this group has done
+    int n_multi = 0;                             // items with >= 2 tiles completed so far
+    Cursor<kGeneral> c;
+    c.init(args, n_items);
+    for (int t = 0; c.valid; ++t, c.next(args)) {
+      const int j = c.j, n = c.it.n;
+      const int n_multi_before = n_multi;
+      const int multi_slot = n_multi & 1;
+      if (j == n - 1 && n >= 2) ++n_multi;
+      if ((t & 1) != g) continue;                // the other group's tile
+      const int buf = t % kSBuf;
+      // Position of this thread's query among the keys.
+      const int qpos = kGeneral ? (args.packed ? r % args.Nq : c.it.qbase + r) + (Nk - args.Nq) : c.it.qbase + r;
+      const uint32_t tS = tmem + buf * 128 + lane_off;
+      if (!mbar_wait_warp(&bars->s_full[buf], (t / kSBuf) & 1, st, abort_flag, kSiteSFull)) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) reg_fence(sr[q]);
+      tc_fence_before();
+      mbar_arrive(&bars->s_free[buf]);   // the MMA may compute S_{t+2} into this buffer now
 
-        const int key0 = (c.it.j0 + j) * kBN;
-        const bool windowed = kGeneral && args.window > 0;
-        if ((key0 + kBN > Nk) || (args.causal && key0 + kBN - 1 > c.it.qmin) ||
-            (windowed && key0 < c.it.qmax - args.window + 1)) {
-          // Keys [key0 + lo, key0 + hi) are visible to this row.
-          const int hi = min(Nk, args.causal ? qpos + 1 : Nk) - key0;
-          const int lo = windowed ? qpos - args.window + 1 - key0 : 0;
-  #pragma unroll
-          for (int q = 0; q < 4; ++q)
-  #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (q * 32 + e >= hi || q * 32 + e < lo) sr[q][e] = __float_as_uint(-INFINITY);
+      const int key0 = (c.it.j0 + j) * kBN;
+      const bool windowed = kGeneral && args.window > 0;
+      if ((key0 + kBN > Nk) || (args.causal && key0 + kBN - 1 > c.it.qmin) ||
+          (windowed && key0 < c.it.qmax - args.window + 1)) {
+        // Keys [key0 + lo, key0 + hi) are visible to this row.
+        const int hi = min(Nk, args.causal ? qpos + 1 : Nk) - key0;
+        const int lo = windowed ? qpos - args.window + 1 - key0 : 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (q * 32 + e >= hi || q * 32 + e < lo) sr[q][e] = __float_as_uint(-INFINITY);
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          mx0 = fmax3(mx0, __uint_as_float(sr[q][e + 0]), __uint_as_float(sr[q][e + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(sr[q][e + 2]), __uint_as_float(sr[q][e + 3]));
+          mx2 = fmax3(mx2, __uint_as_float(sr[q][e + 4]), __uint_as_float(sr[q][e + 5]));
+          mx3 = fmax3(mx3, __uint_as_float(sr[q][e + 6]), __uint_as_float(sr[q][e + 7]));
         }
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-  #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-  #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            mx0 = fmax3(mx0, __uint_as_float(sr[q][e + 0]), __uint_as_float(sr[q][e + 1]));
-            mx1 = fmax3(mx1, __uint_as_float(sr[q][e + 2]), __uint_as_float(sr[q][e + 3]));
-            mx2 = fmax3(mx2, __uint_as_float(sr[q][e + 4]), __uint_as_float(sr[q][e + 5]));
-            mx3 = fmax3(mx3, __uint_as_float(sr[q][e + 6]), __uint_as_float(sr[q][e + 7]));
+      }
+      const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      // Reference max after the previous tile (owned by the other group).  The
+      // wait also happens at an item's first tile, where the value is unused:
+      // it keeps the two groups' hand-offs strictly alternating, so no hand
+      // barrier can run two phases ahead of its waiter.
+      float m_prev = -INFINITY;
+      if (t > 0) {
+        if (!mbar_wait_warp(&bars->hand[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteHand)) break;
+        if (j > 0) m_prev = mref[((t - 1) & 1) * 128 + r];
+      }
+      const bool need = (j == 0) || (m_cand > m_prev + kRescaleThreshold);
+      const float m_new = need ? m_cand : m_prev;
+      // Hand the reference on to the owner of tile t+1 right away.
+      mref[(t & 1) * 128 + r] = m_new;
+      mbar_arrive(&bars->hand[t & 1]);
+
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      if (my_item != c.item) {
+        my_item = c.item;
+        l_g = 0.f;
+      } else if (m_g != m_new) {
+        l_g *= ex2(m_g - m_use);
+      }
+      m_g = m_new;
+
+      // P = 2^(s*sl2 - m), 32 keys at a time, into probability buffer t % 2
+      // once P V_{t-2} has consumed it.
+      if (t >= 2 && !mbar_wait_warp(&bars->o_done[t & 1], ((t >> 1) - 1) & 1, st, abort_flag, kSitePPrev)) break;
+      tc_fence_after();
+      const uint32_t tP = tmem + 256 + buf * 64 + lane_off;
+      const uint64_t negm = f2pack(-m_use, -m_use);
+      uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint64_t x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint64_t sv = f2pack(__uint_as_float(sr[q][e + 2 * u]), __uint_as_float(sr[q][e + 2 * u + 1]));
+            float lo, hi;
+            f2unpack(ffma2(sv, sl2x2, negm), lo, hi);
+            lo = ex2(lo);
+            hi = ex2(hi);
+            x[u] = f2pack(lo, hi);
+            pk[e / 2 + u] = cvt_bf16x2(lo, hi);
           }
+          acc0 = fadd2(acc0, x[0]);
+          acc1 = fadd2(acc1, x[1]);
+          acc2 = fadd2(acc2, x[2]);
+          acc3 = fadd2(acc3, x[3]);
         }
-        const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-        // Reference max after the previous tile (owned by the other group).  The
-        // wait also happens at an item's first tile, where the value is unused:
-        // it keeps the two groups' hand-offs strictly alternating, so no hand
-        // barrier can run two phases ahead of its waiter.
-        float m_prev = -INFINITY;
-        if (t > 0) {
-          if (!mbar_wait_warp(&bars->hand[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteHand)) break;
-          if (j > 0) m_prev = mref[((t - 1) & 1) * 128 + r];
-        }
-        const bool need = (j == 0) || (m_cand > m_prev + kRescaleThreshold);
-        const float m_new = need ? m_cand : m_prev;
-        // Hand the reference on to the owner of tile t+1 right away.
-        mref[(t & 1) * 128 + r] = m_new;
-        mbar_arrive(&bars->hand[t & 1]);
+        tmem_st16(tP + q * 16, pk);
+      }
+      float a0, a1;
+      f2unpack(fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3)), a0, a1);
+      l_g += a0 + a1;
 
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        if (my_item != c.item) {
-          my_item = c.item;
-          l_g = 0.f;
-        } else if (m_g != m_new) {
-          l_g *= ex2(m_g - m_use);
-        }
-        m_g = m_new;
-
-        // P = 2^(s*sl2 - m), 32 keys at a time, into probability buffer t % 2
-        // once P V_{t-2} has consumed it.
-        if (t >= 2 && !mbar_wait_warp(&bars->o_done[t & 1], ((t >> 1) - 1) & 1, st, abort_flag, kSitePPrev)) break;
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O holds rows relative to the previous reference: rescale it once
+        // P V of the previous tile has landed.
+        const float alpha = need ? ex2(m_prev - m_use) : 1.f;
+        if (!mbar_wait_warp(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteORescale)) break;
         tc_fence_after();
-        const uint32_t tP = tmem + 256 + buf * 64 + lane_off;
-        const uint64_t negm = f2pack(-m_use, -m_use);
-        uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
-  #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t pk[16];
-  #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint64_t x[4];
-  #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint64_t sv = f2pack(__uint_as_float(sr[q][e + 2 * u]), __uint_as_float(sr[q][e + 2 * u + 1]));
-              float lo, hi;
-              f2unpack(ffma2(sv, sl2x2, negm), lo, hi);
-              lo = ex2(lo);
-              hi = ex2(hi);
-              x[u] = f2pack(lo, hi);
-              pk[e / 2 + u] = cvt_bf16x2(lo, hi);
-            }
-            acc0 = fadd2(acc0, x[0]);
-            acc1 = fadd2(acc1, x[1]);
-            acc2 = fadd2(acc2, x[2]);
-            acc3 = fadd2(acc3, x[3]);
+        const uint64_t al2 = f2pack(alpha, alpha);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tO + lane_off + q * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float lo, hi;
+            f2unpack(fmul2(f2pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), al2), lo, hi);
+            o[e] = __float_as_uint(lo);
+            o[e + 1] = __float_as_uint(hi);
           }
-          tmem_st16(tP + q * 16, pk);
+          tmem_st32(tO + lane_off + q * 32, o);
         }
-        float a0, a1;
-        f2unpack(fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3)), a0, a1);
-        l_g += a0 + a1;
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[buf]);
 
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-          // O holds rows relative to the previous reference: rescale it once
-          // P V of the previous tile has landed.
-          const float alpha = need ? ex2(m_prev - m_use) : 1.f;
-          if (!mbar_wait_warp(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteORescale)) break;
-          tc_fence_after();
-          const uint64_t al2 = f2pack(alpha, alpha);
-  #pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t o[32];
-            tmem_ld32(tO + lane_off + q * 32, o);
+      if (j == n - 2) {
+        // The other group owns the item's last tile: hand it this group's
+        // row-sum part, relative to m_new (which it reads back as m_prev).
+        lxb[multi_slot * 128 + r] = l_g;
+        mbar_arrive(&bars->lx[multi_slot]);
+      }
+      if (j == n - 1) {
+        // ------------------------------------------------ epilogue of the item
+        float l_tot = l_g;
+        if (n >= 2) {
+          if (!mbar_wait_warp(&bars->lx[multi_slot], (n_multi_before >> 1) & 1, st, abort_flag, kSiteLx)) break;
+          l_tot += lxb[multi_slot * 128 + r] * ex2(m_prev - m_use);
+        }
+        if (!mbar_wait_warp(&bars->o_done[t & 1], (t >> 1) & 1, st, abort_flag, kSiteOLast)) break;
+        tc_fence_after();
+        const long long frow = c.it.row0 + r;
+        if constexpr (!kGeneral) {
+          // Plain instance: every thread writes its O row, normalised to
+          // bf16, into the item's Q slot (free: the item's last S has
+          // completed), 128-byte swizzled like the tensor map's box, 64
+          // columns at a time; one thread then writes the tile with TMA
+          // stores (rows past N are clipped) -- far cheaper for the group
+          // than 128 threads storing one row each.
+          const float inv_l = 1.f / l_tot;
+          const uint32_t stage = smem_u32(smem + L::kQ) + (c.li & 1) * L::kTile;
+#pragma unroll
+          for (int a = 0; a < kAtoms; ++a) {
+            uint32_t o[2][32];
+            tmem_ld32(tO + lane_off + a * 64, o[0]);
+            tmem_ld32(tO + lane_off + a * 64 + 32, o[1]);
             tmem_wait_ld();
-            reg_fence(o);
-  #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float lo, hi;
-              f2unpack(fmul2(f2pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), al2), lo, hi);
-              o[e] = __float_as_uint(lo);
-              o[e + 1] = __float_as_uint(hi);
-            }
-            tmem_st32(tO + lane_off + q * 32, o);
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->p_full[buf]);
-
-        if (j == n - 2) {
-          // The other group owns the item's last tile: hand it this group's
-          // row-sum part, relative to m_new (which it reads back as m_prev).
-          lxb[multi_slot * 128 + r] = l_g;
-          mbar_arrive(&bars->lx[multi_slot]);
-        }
-        if (j == n - 1) {
-          // ------------------------------------------------ epilogue of the item
-          float l_tot = l_g;
-          if (n >= 2) {
-            if (!mbar_wait_warp(&bars->lx[multi_slot], (n_multi_before >> 1) & 1, st, abort_flag, kSiteLx)) break;
-            l_tot += lxb[multi_slot * 128 + r] * ex2(m_prev - m_use);
-          }
-          if (!mbar_wait_warp(&bars->o_done[t & 1], (t >> 1) & 1, st, abort_flag, kSiteOLast)) break;
-          tc_fence_after();
-          const long long frow = c.it.row0 + r;
-          if (!kGeneral) {
-            // Plain instance: every thread writes its O row, normalised to
-            // bf16, into the item's Q slot (free: the item's last S has
-            // completed), 128-byte swizzled like the tensor map's box, 64
-            // columns at a time; one thread then writes the tile with TMA
-            // stores (rows past N are clipped) -- far cheaper for the group
-            // than 128 threads storing one row each.
-            const float inv_l = 1.f / l_tot;
-            const uint32_t stage = smem_u32(smem + L::kQ) + (c.li & 1) * L::kTile;
-  #pragma unroll
-            for (int a = 0; a < kAtoms; ++a) {
-              uint32_t o[2][32];
-              tmem_ld32(tO + lane_off + a * 64, o[0]);
-              tmem_ld32(tO + lane_off + a * 64 + 32, o[1]);
-              tmem_wait_ld();
-              reg_fence(o[0]);
-              reg_fence(o[1]);
-  #pragma unroll
-              for (int q = 0; q < 2; ++q) {
-  #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                  const uint32_t w0 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 0]) * inv_l, __uint_as_float(o[q][v * 8 + 1]) * inv_l);
-                  const uint32_t w1 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 2]) * inv_l, __uint_as_float(o[q][v * 8 + 3]) * inv_l);
-                  const uint32_t w2 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 4]) * inv_l, __uint_as_float(o[q][v * 8 + 5]) * inv_l);
-                  const uint32_t w3 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 6]) * inv_l, __uint_as_float(o[q][v * 8 + 7]) * inv_l);
-                  // Columns a*64 + q*32 + v*8 .. +7: block a, 16-byte chunk q*4 + v.
-                  st_shared_v4(stage + a * kBlockBytes + swz128(r, q * 4 + v), w0, w1, w2, w3);
-                }
+            reg_fence(o[0]);
+            reg_fence(o[1]);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const uint32_t w0 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 0]) * inv_l, __uint_as_float(o[q][v * 8 + 1]) * inv_l);
+                const uint32_t w1 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 2]) * inv_l, __uint_as_float(o[q][v * 8 + 3]) * inv_l);
+                const uint32_t w2 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 4]) * inv_l, __uint_as_float(o[q][v * 8 + 5]) * inv_l);
+                const uint32_t w3 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 6]) * inv_l, __uint_as_float(o[q][v * 8 + 7]) * inv_l);
+                // Columns a*64 + q*32 + v*8 .. +7: block a, 16-byte chunk q*4 + v.
+                st_shared_v4(stage + a * kBlockBytes + swz128(r, q * 4 + v), w0, w1, w2, w3);
               }
             }
-            tc_fence_before();
-            mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
-            if (r < c.it.rows) args.lse[frow] = (m_new + __log2f(l_tot)) * 0.69314718055994530942f;
-            fence_proxy_async_smem();
-            mbar_arrive(&bars->stg_full[g]);
-            if (quad == 0 && lane == 0) {
-              if (!mbar_wait(&bars->stg_full[g], n_epi & 1, st, abort_flag, kSiteOLast)) break;
-  #pragma unroll
-              for (int a = 0; a < kAtoms; ++a)
-                tma_store_4d(&tmO, stage + a * kBlockBytes, a * 64, c.it.qbase, c.it.h, c.it.b);
-              bulk_commit_group();
-              bulk_wait_read<0>();   // the Q slot may be reloaded once TMA has read the staging
-              mbar_arrive(&bars->q_empty[c.li & 1]);
-            }
-            ++n_epi;
-            continue;
           }
+          tc_fence_before();
+          mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
+          if (r < c.it.rows) args.lse[frow] = (m_new + __log2f(l_tot)) * 0.69314718055994530942f;
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->stg_full[g]);
+          if (quad == 0 && lane == 0) {
+            if (!mbar_wait(&bars->stg_full[g], n_epi & 1, st, abort_flag, kSiteOLast)) break;
+#pragma unroll
+            for (int a = 0; a < kAtoms; ++a)
+              tma_store_4d(&tmO, stage + a * kBlockBytes, a * 64, c.it.qbase, c.it.h, c.it.b);
+            bulk_commit_group();
+            bulk_wait_read<0>();   // the Q slot may be reloaded once TMA has read the staging
+            mbar_arrive(&bars->q_empty[c.li & 1]);
+          }
+          ++n_epi;
+        } else {
           uint32_t o[D / 32][32];
-  #pragma unroll
+#pragma unroll
           for (int q = 0; q < D / 32; ++q) tmem_ld32(tO + lane_off + q * 32, o[q]);
           tmem_wait_ld();
-  #pragma unroll
+#pragma unroll
           for (int q = 0; q < D / 32; ++q) reg_fence(o[q]);
           tc_fence_before();
           mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
@@ -610,9 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (args.splits == 1) {
               const float inv_l = 1.f / l_tot;
               __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.o) + frow * D;
-  #pragma unroll
+#pragma unroll
               for (int q = 0; q < D / 32; ++q) {
-  #pragma unroll
+#pragma unroll
                 for (int v = 0; v < 4; ++v) {
                   uint4 w;
                   w.x = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 0]) * inv_l, __uint_as_float(o[q][v * 8 + 1]) * inv_l);
@@ -629,9 +628,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const long long prow = (long long)c.it.split * args.B * args.Hq * args.Nq + frow;
               const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
               float4* orow = reinterpret_cast<float4*>(args.o_part + prow * D);
-  #pragma unroll
+#pragma unroll
               for (int q = 0; q < D / 32; ++q)
-  #pragma unroll
+#pragma unroll
                 for (int v = 0; v < 8; ++v)
                   orow[q * 8 + v] = make_float4(__uint_as_float(o[q][v * 4 + 0]) * inv_l,
                                                 __uint_as_float(o[q][v * 4 + 1]) * inv_l,
@@ -643,6 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+    }
   }
 
   // TMA stores of the O epilogue must be complete before the CTA exits.
