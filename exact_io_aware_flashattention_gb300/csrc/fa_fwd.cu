@@ -78,7 +78,7 @@ struct FwdCfg {
 // Wait-site ids reported in the status words.
 enum : int {
   kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSitePFull, kSiteVFull, kSiteOFree,
-  kSiteSFree, kSiteSFull, kSiteORescale, kSiteOLast, kSiteHand, kSiteLx, kSitePPrev
+  kSiteSFree, kSiteSFull, kSiteORescale, kSiteOLast, kSiteHand, kSiteLx, kSitePPrev, kSiteOStaged
 };
 
 struct Bars {
@@ -91,7 +91,7 @@ struct Bars {
   uint64_t hand[2];         // reference max of tile t published (by tile parity)
   uint64_t lx[2];           // row-sum part of the non-owner group published (by multi-tile item parity)
   uint64_t drain_s, drain_pv;
-  uint64_t stg_full[2];     // per softmax group: the O staging of its epilogue is written
+  uint64_t o_staged[2];     // per Q slot: the finished item's O is staged in the slot (plain instance)
   uint32_t tmem_base;
   int abort;
 };
@@ -228,9 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1);
-      // Last S of the item done (+ in the plain instance, the O epilogue's
-      // TMA store has read its staging, which reuses the item's Q slot).
-      mbar_init(&bars->q_empty[i], kGeneral ? 1 : 2);
+      mbar_init(&bars->q_empty[i], 1);   // last S of the item done (general instance)
       mbar_init(&bars->o_done[i], 1);
       mbar_init(&bars->hand[i], 128);
       mbar_init(&bars->lx[i], 128);
@@ -251,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->o_free, 128);
     mbar_init(&bars->drain_s, 1);
     mbar_init(&bars->drain_pv, 1);
-    for (int x = 0; x < 2; ++x) mbar_init(&bars->stg_full[x], 128);
+    for (int x = 0; x < 2; ++x) mbar_init(&bars->o_staged[x], 128);
     bars->abort = 0;
     mbar_fence_init();
     fence_proxy_async_smem();
@@ -281,12 +279,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         int kt = 0, li = 0;
         int q_issued[2] = {0, 0};
+        int o_qbase[2] = {0, 0}, o_h[2] = {0, 0}, o_b[2] = {0, 0};   // O tile of the item in each Q slot
+        // Plain instance: the softmax group that finishes item k stages its O
+        // in the item's Q slot; this thread writes it out with TMA stores and
+        // reloads the slot once they have read it, so that the softmax warps
+        // never wait for the store.
+        auto store_o = [&](int k) -> bool {
+          const int sl = k & 1;
+          if (!mbar_wait(&bars->o_staged[sl], (k >> 1) & 1, st, abort_flag, kSiteOStaged)) return false;
+          for (int a = 0; a < kAtoms; ++a)
+            tma_store_4d(&tmO, sQ + sl * L::kTile + a * kBlockBytes, a * 64, o_qbase[sl], o_h[sl], o_b[sl]);
+          bulk_commit_group();
+          bulk_wait_read<0>();
+          return true;
+        };
         bool ok = true;
         for (int round = 0, item = item_of_round(0); ok && item < n_items; item = item_of_round(++round)) {
           const Item it = decode_item<kGeneral>(item, args);
           if (it.n == 0) continue;
           const int slot = li & 1;
-          if (li >= 2 && !mbar_wait(&bars->q_empty[slot], ((li >> 1) - 1) & 1, st, abort_flag, kSiteQEmpty)) break;
+          if (li >= 2) {
+            if constexpr (kGeneral) {
+              if (!mbar_wait(&bars->q_empty[slot], ((li >> 1) - 1) & 1, st, abort_flag, kSiteQEmpty)) { ok = false; break; }
+            } else {
+              if (!store_o(li - 2)) { ok = false; break; }
+            }
+          }
+          o_qbase[slot] = it.qbase;
+          o_h[slot] = it.h;
+          o_b[slot] = it.b;
           mbar_arrive_expect_tx(&bars->q_full[slot], L::kTile);
           for (int a = 0; a < kAtoms; ++a)
             tma_load_3d(smem + L::kQ + slot * L::kTile + a * kBlockBytes, &tmQ, &bars->q_full[slot], a * 64,
@@ -301,6 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                           (it.j0 + j) * kBN, it.kvh, it.b);
           }
           ++li;   // items with key tiles, in the order the MMA issuers' cursors count them
+        }
+        if constexpr (!kGeneral) {
+          // The last two items' O, then every store complete before the CTA exits.
+          for (int k = li >= 2 ? li - 2 : 0; ok && k < li; ++k) ok = store_o(k);
+          bulk_wait_all();
         }
         // Every copy issued must have landed before the CTA may exit.
         for (int i = 0; i < 2; ++i)
@@ -400,7 +426,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_g = -INFINITY;                       // reference max this group's row sum is relative to
     float l_g = 0.f;                             // this group's part of the row sum
     int my_item = -1;                            // item the group's (l_g, m_g) belong to
-    int n_epi = 0;                               // item epilogues this group has done
     int n_multi = 0;                             // items with >= 2 tiles completed so far
     Cursor<kGeneral> c;
     c.init(args, n_items);
@@ -555,9 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Plain instance: every thread writes its O row, normalised to
           // bf16, into the item's Q slot (free: the item's last S has
           // completed), 128-byte swizzled like the tensor map's box, 64
-          // columns at a time; one thread then writes the tile with TMA
-          // stores (rows past N are clipped) -- far cheaper for the group
-          // than 128 threads storing one row each.
+          // columns at a time; the Q / K producer then writes the tile with
+          // TMA stores (rows past N are clipped) before it reloads the slot.
+          // The group neither stores rows nor waits for the store.
           const float inv_l = 1.f / l_tot;
           const uint32_t stage = smem_u32(smem + L::kQ) + (c.li & 1) * L::kTile;
 #pragma unroll
@@ -585,17 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
           if (r < c.it.rows) args.lse[frow] = (m_new + __log2f(l_tot)) * 0.69314718055994530942f;
           fence_proxy_async_smem();
-          mbar_arrive(&bars->stg_full[g]);
-          if (quad == 0 && lane == 0) {
-            if (!mbar_wait(&bars->stg_full[g], n_epi & 1, st, abort_flag, kSiteOLast)) break;
-#pragma unroll
-            for (int a = 0; a < kAtoms; ++a)
-              tma_store_4d(&tmO, stage + a * kBlockBytes, a * 64, c.it.qbase, c.it.h, c.it.b);
-            bulk_commit_group();
-            bulk_wait_read<0>();   // the Q slot may be reloaded once TMA has read the staging
-            mbar_arrive(&bars->q_empty[c.li & 1]);
-          }
-          ++n_epi;
+          mbar_arrive(&bars->o_staged[c.li & 1]);   // the Q / K producer stores it
         } else {
           uint32_t o[D / 32][32];
 #pragma unroll
@@ -645,8 +660,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // TMA stores of the O epilogue must be complete before the CTA exits.
-  if (!kGeneral) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
