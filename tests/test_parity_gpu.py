@@ -112,6 +112,21 @@ def test_head_groupings(cuda_lib, B, Hq, Hkv, N, d, causal):
     assert_bwd(dq, dk, dv, rdq, rdk, rdv)
 
 
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+def test_many_items_per_cta_ragged(cuda_lib, d, causal):
+    """More (query tile, head) items than SMs with a ragged last tile, so every
+    persistent CTA finishes several items whose O goes out through the Q slot
+    it is staged in, partial tiles included, and each dK/dV CTA walks several
+    units."""
+    B, Hq, Hkv, N = 4, 12, 12, 1000
+    q, k, v, do = make_qkvdo(B, Hq, Hkv, N, d, seed=4000 + d)
+    scale = 1.0 / np.sqrt(d)
+    o, lse, dq, dk, dv = run_gpu(q, k, v, do, causal, scale)
+    ro, rlse, rdq, rdk, rdv = oracle(q, k, v, do, causal, scale)
+    assert_fwd(o, lse, ro, rlse, f"many items d={d} causal={causal}")
+    assert_bwd(dq, dk, dv, rdq, rdk, rdv, f"many items d={d} causal={causal}")
+
+
 def test_gqa_equals_repeated_heads_on_gpu(cuda_lib):
     # Grouped attention == multi-head attention on K/V repeated per group.
     B, Hq, Hkv, N, d = 1, 8, 2, 640, 128
