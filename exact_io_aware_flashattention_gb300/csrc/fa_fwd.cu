@@ -9,8 +9,11 @@
 // accumulate P V.  O / l and LSE = m + ln l are written once at the end.
 // Multiplying numerator and denominator by one factor leaves their ratio
 // unchanged ([Lecture], same section), so the reference max may lag the true
-// max: it is only raised when the true max exceeds it by more than 2^8 (log2
-// units), which keeps every exponent <= 2^8 and skips most rescales.
+// max: it is only raised when the true max exceeds it by more than 24 (log2
+// units).  Every unnormalised probability then stays <= 2^24, a row sum
+// <= N * 2^24 and an O entry <= N * 2^24 * max|V| (fp32 holds that for |V|
+// up to ~1e24 at N = 8M), and rows whose max keeps climbing, as with large
+// score spreads, rescale O in tensor memory only a few times.
 //
 // Persistent kernel: one CTA per SM walks work items (query tile, head,
 // batch), heaviest causal tiles first, dealt to the CTAs in snake order.  CTA layout (384 threads):
@@ -59,7 +62,7 @@ constexpr int kCtrlRegs = 56;
 constexpr int kSoftmaxRegs = (kLaunchRegs * 3 - kCtrlRegs) / 2;   // 224: the shares add up to the launch allocation
 static_assert(kSoftmaxRegs % 8 == 0 && kSoftmaxRegs <= 256, "register split");
 constexpr uint32_t kBlockBytes = 128u * 128u;   // one 64-column block of a 128-row bf16 tile
-constexpr float kRescaleThreshold = 8.0f;
+constexpr float kRescaleThreshold = 24.0f;   // log2 units; see the header
 
 template <int D>
 struct FwdCfg {
