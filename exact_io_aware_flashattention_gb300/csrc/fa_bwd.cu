@@ -282,6 +282,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);   // S^T, dP^T
       constexpr uint32_t idKM = idesc_bf16(128, D, false, true);      // dV, dK
       constexpr uint32_t idMM = idesc_bf16(128, D, true, true);       // dQ
+      // Operand descriptors, built once: a k16 step adds a constant.
+      const uint64_t dKk = desc_kmajor(sK, 0, kBlockBytes), dVk = desc_kmajor(sV, 0, kBlockBytes);
+      const uint64_t dKm = desc_mnmajor(sK, 0, kBlockBytes), dDSm = desc_mnmajor(sDS, 0, kBlockBytes);
+      const uint64_t dQk0 = desc_kmajor(sQ, 0, kBlockBytes), dQk1 = desc_kmajor(sQ + L::kTile, 0, kBlockBytes);
+      const uint64_t dOk0 = desc_kmajor(sDO, 0, kBlockBytes), dOk1 = desc_kmajor(sDO + L::kTile, 0, kBlockBytes);
+      const uint64_t dQm0 = desc_mnmajor(sQ, 0, kBlockBytes), dQm1 = desc_mnmajor(sQ + L::kTile, 0, kBlockBytes);
+      const uint64_t dOm0 = desc_mnmajor(sDO, 0, kBlockBytes), dOm1 = desc_mnmajor(sDO + L::kTile, 0, kBlockBytes);
       bool ok = true;
       int T = 0, nu = 0;
       for (int round = 0; ok; ++round, ++nu) {
@@ -295,7 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sph = (tg >> 1) & 1;  // slot phase
         const uint32_t ph = tg & 1;          // per-item barrier phase
         const uint32_t pph = (tg - 1) & 1;   // previous item's phase
-        const uint32_t qa = sQ + slot * L::kTile, da = sDO + slot * L::kTile;
+        const uint64_t dQk = slot ? dQk1 : dQk0, dOk = slot ? dOk1 : dOk0;
+        const uint64_t dQm = slot ? dQm1 : dQm0, dOm = slot ? dOm1 : dOm0;
         if (!mbar_wait(&bars->q_full[slot], sph, st, abort_flag, kSiteQFull)) { ok = false; break; }
         // S_{t+1} overwrites the score region, which holds P^T_t (read by dV_t)
         // and dS^T_t (read by dK_t); dK_t is the later of the two.
@@ -303,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
-          mma_bf16_ss(tS, desc_kmajor(sK, k16, kBlockBytes), desc_kmajor(qa, k16, kBlockBytes), idSS, k16 > 0);
+          mma_bf16_ss(tS, dKk + desc_step_kmajor(k16, kBlockBytes), dQk + desc_step_kmajor(k16, kBlockBytes), idSS,
+                      k16 > 0);
         mma_commit(&bars->s_full);
         if (!mbar_wait(&bars->do_full[slot], sph, st, abort_flag, kSiteDoFull)) { ok = false; break; }
         // dP_t overwrites the dQ partial of item t-1 (read out by then) or,
@@ -312,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
-          mma_bf16_ss(tDP, desc_kmajor(sV, k16, kBlockBytes), desc_kmajor(da, k16, kBlockBytes), idSS, k16 > 0);
+          mma_bf16_ss(tDP, dVk + desc_step_kmajor(k16, kBlockBytes), dOk + desc_step_kmajor(k16, kBlockBytes), idSS,
+                      k16 > 0);
         mma_commit(&bars->dp_full);
         if (!mbar_wait(&bars->p_full, ph, st, abort_flag, kSitePFull)) { ok = false; break; }
         // The unit's first dV / dK overwrite the previous unit's accumulators:
@@ -325,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P^T for query columns 16*k16.. lives at column (k16/4)*64 + (k16%4)*8.
 #pragma unroll
         for (int k16 = 0; k16 < kT / 16; ++k16)
-          mma_bf16_ts(tDV, tS + (k16 >> 2) * 64 + (k16 & 3) * 8, desc_mnmajor(da, k16, kBlockBytes), idKM,
+          mma_bf16_ts(tDV, tS + (k16 >> 2) * 64 + (k16 & 3) * 8, dOm + desc_step_mnmajor(k16), idKM,
                       (t > 0 || k16 > 0) ? 1u : 0u);
         mma_commit(&bars->do_empty[slot]);
         if (!mbar_wait(&bars->ds_full, ph, st, abort_flag, kSiteDsFull)) { ok = false; break; }
@@ -333,13 +343,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dS^T for query columns 16*k16.. lives at column (k16/4)*64 + 32 + (k16%4)*8.
 #pragma unroll
         for (int k16 = 0; k16 < kT / 16; ++k16)
-          mma_bf16_ts(tDK, tS + (k16 >> 2) * 64 + 32 + (k16 & 3) * 8, desc_mnmajor(qa, k16, kBlockBytes), idKM,
+          mma_bf16_ts(tDK, tS + (k16 >> 2) * 64 + 32 + (k16 & 3) * 8, dQm + desc_step_mnmajor(k16), idKM,
                       (t > 0 || k16 > 0) ? 1u : 0u);
         mma_commit(&bars->dk_done);
         if (kDq) {
 #pragma unroll
           for (int k16 = 0; k16 < kT / 16; ++k16)
-            mma_bf16_ss(tDP, desc_mnmajor(sDS, k16, kBlockBytes), desc_mnmajor(sK, k16, kBlockBytes), idMM,
+            mma_bf16_ss(tDP, dDSm + desc_step_mnmajor(k16), dKm + desc_step_mnmajor(k16), idMM,
                         k16 > 0 ? 1u : 0u);
           mma_commit(&bars->dq_full);
         }

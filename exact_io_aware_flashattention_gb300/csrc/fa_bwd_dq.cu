@@ -175,17 +175,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);   // S, dP
       constexpr uint32_t idQ = idesc_bf16(128, D, false, true);       // dQ += dS K (K as the MN-major operand)
+      // Operand descriptors, built once: a K / V stage or a k16 step adds a constant.
+      const uint64_t dQk = desc_kmajor(sQ, 0, kBlockBytes), dOk = desc_kmajor(sDO, 0, kBlockBytes);
+      const uint64_t dKk = desc_kmajor(sK, 0, kBlockBytes), dKm = desc_mnmajor(sK, 0, kBlockBytes);
+      const uint64_t dVk = desc_kmajor(sV, 0, kBlockBytes);
       // dQ_j: A = dS_j in S buffer j % 2 (group g's keys at columns 64g..),
       // B = K_j; releases the K stage afterwards.
       auto issue_dq = [&](int jj) -> bool {
         const int x = jj & 1, s = jj % SK;
         if (!mbar_wait(&bars->ds_full[x], (jj >> 1) & 1, st, abort_flag, kSiteDsFull)) return false;
         tc_fence_after();
-        const uint32_t ka = sK + s * L::kTile;
+        const uint64_t dk = dKm + (uint64_t)s * (L::kTile >> 4);
 #pragma unroll
         for (int k16 = 0; k16 < kT / 16; ++k16)
-          mma_bf16_ts(tDQ, tmem + x * 128 + (k16 >> 2) * 64 + (k16 & 3) * 8, desc_mnmajor(ka, k16, kBlockBytes),
-                      idQ, (jj > 0 || k16 > 0) ? 1u : 0u);
+          mma_bf16_ts(tDQ, tmem + x * 128 + (k16 >> 2) * 64 + (k16 & 3) * 8, dk + desc_step_mnmajor(k16), idQ,
+                      (jj > 0 || k16 > 0) ? 1u : 0u);
         mma_commit(&bars->dq_done[x]);
         mma_commit(&bars->k_empty[s]);
         return true;
@@ -197,20 +201,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (jj >= 2 && !mbar_wait(&bars->dq_done[x], ((jj - 2) >> 1) & 1, st, abort_flag, kSiteDqDone)) break;
         if (!mbar_wait(&bars->k_full[s], (jj / SK) & 1, st, abort_flag, kSiteKFull)) break;
         tc_fence_after();
-        const uint32_t ka = sK + s * L::kTile;
+        const uint64_t dk = dKk + (uint64_t)s * (L::kTile >> 4);
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
-          mma_bf16_ss(tmem + x * 128, desc_kmajor(sQ, k16, kBlockBytes), desc_kmajor(ka, k16, kBlockBytes), idSS,
-                      k16 > 0);
+          mma_bf16_ss(tmem + x * 128, dQk + desc_step_kmajor(k16, kBlockBytes), dk + desc_step_kmajor(k16, kBlockBytes),
+                      idSS, k16 > 0);
         mma_commit(&bars->s_full[x]);
         // dP_jj overwrites dP_{jj-1}: the compute threads must have read it.
         if (jj >= 1 && !mbar_wait(&bars->dp_free, (jj - 1) & 1, st, abort_flag, kSiteDpFree)) break;
         if (!mbar_wait(&bars->v_full[s], (jj / SK) & 1, st, abort_flag, kSiteVFull)) break;
         tc_fence_after();
-        const uint32_t va = sV + s * L::kTile;
+        const uint64_t dv = dVk + (uint64_t)s * (L::kTile >> 4);
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
-          mma_bf16_ss(tDP, desc_kmajor(sDO, k16, kBlockBytes), desc_kmajor(va, k16, kBlockBytes), idSS, k16 > 0);
+          mma_bf16_ss(tDP, dOk + desc_step_kmajor(k16, kBlockBytes), dv + desc_step_kmajor(k16, kBlockBytes), idSS,
+                      k16 > 0);
         mma_commit(&bars->dp_full);
         mma_commit(&bars->v_empty[s]);
         if (jj >= 1 && !issue_dq(jj - 1)) break;

@@ -364,6 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------ S issuer
       if (lane == 0) {
         constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+        // Operand descriptors, built once: a K stage or a k16 step adds a constant.
+        const uint64_t dQ0 = desc_kmajor(sQ, 0, kBlockBytes), dQ1 = desc_kmajor(sQ + L::kTile, 0, kBlockBytes);
+        const uint64_t dK0 = desc_kmajor(sK, 0, kBlockBytes);
         Cursor<kGeneral> sc;
         sc.init(args, n_items);
         for (int ts = 0; sc.valid; ++ts, sc.next(args)) {
@@ -376,12 +379,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = ts % SK;
           if (!mbar_wait(&bars->k_full[s], (ts / SK) & 1, st, abort_flag, kSiteKFull)) break;
           tc_fence_after();
-          const uint32_t qa = sQ + (sc.li & 1) * L::kTile;
-          const uint32_t ka = sK + s * L::kTile;
+          const uint64_t dq = (sc.li & 1) ? dQ1 : dQ0;
+          const uint64_t dk = dK0 + (uint64_t)s * (L::kTile >> 4);
 #pragma unroll
           for (int k16 = 0; k16 < D / 16; ++k16)
-            mma_bf16_ss(tmem + buf * 128, desc_kmajor(qa, k16, kBlockBytes), desc_kmajor(ka, k16, kBlockBytes), idS,
-                        k16 > 0);
+            mma_bf16_ss(tmem + buf * 128, dq + desc_step_kmajor(k16, kBlockBytes), dk + desc_step_kmajor(k16, kBlockBytes),
+                        idS, k16 > 0);
           mma_commit(&bars->s_full[buf]);
           mma_commit(&bars->k_empty[s]);
           if (sc.j == sc.it.n - 1) mma_commit(&bars->q_empty[sc.li & 1]);
@@ -394,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------ P V issuer
       if (lane == 0) {
         constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
+        const uint64_t dV0 = desc_mnmajor(sV, 0, kBlockBytes);
         Cursor<kGeneral> pc;
         pc.init(args, n_items);
         for (int t = 0; pc.valid; ++t, pc.next(args)) {
@@ -403,10 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&bars->v_full[v], (t / SV) & 1, st, abort_flag, kSiteVFull)) break;
           if (pc.j == 0 && pc.li > 0 && !mbar_wait(&bars->o_free, (pc.li - 1) & 1, st, abort_flag, kSiteOFree)) break;
           tc_fence_after();
-          const uint32_t va = sV + v * L::kTile;
+          const uint64_t dv = dV0 + (uint64_t)v * (L::kTile >> 4);
 #pragma unroll
           for (int k16 = 0; k16 < kBN / 16; ++k16)
-            mma_bf16_ts(tO, tmem + 256 + buf * 64 + k16 * 8, desc_mnmajor(va, k16, kBlockBytes), idO,
+            mma_bf16_ts(tO, tmem + 256 + buf * 64 + k16 * 8, dv + desc_step_mnmajor(k16), idO,
                         (pc.j > 0 || k16 > 0) ? 1u : 0u);
           mma_commit(&bars->o_done[t & 1]);
           mma_commit(&bars->v_empty[v]);

@@ -344,6 +344,14 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_addr, int k16, uin
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_addr, int k16, uint32_t block_bytes) {
   return sdesc_sw128(tile_addr + (uint32_t)k16 * 2048u, block_bytes, 1024u);
 }
+// Start-address offset (16-byte units) of k16 step `k16` inside a 128-byte
+// swizzled operand tile: the descriptor of the step is the tile's k16 = 0
+// descriptor plus this constant (the address field cannot overflow: shared
+// memory addresses stay below 2^18).
+__host__ __device__ constexpr uint64_t desc_step_kmajor(int k16, uint32_t block_bytes) {
+  return (uint64_t)(((uint32_t)(k16 >> 2) * block_bytes + (uint32_t)(k16 & 3) * 32u) >> 4);
+}
+__host__ __device__ constexpr uint64_t desc_step_mnmajor(int k16) { return (uint64_t)((uint32_t)k16 * 2048u >> 4); }
 
 // ---------------------------------------------------------------------------
 // Math helpers
