@@ -7,7 +7,9 @@ d=128).
 Prints ONE JSON line (rank 0).  `value` is TFLOPS under the convention
 fwd = 4*B*Hq*N^2*d (halved when causal), bwd = 2.5 x fwd, over the device time
 of the K timed steps (CUDA events around each step on the launching stream;
-L2 is flushed by a 256 MiB write between steps, outside the events).
+between steps, outside the events, L2 is flushed by a 256 MiB write and then
+a 256 MiB read of another buffer, so each step starts from a cold and clean
+L2 instead of writing back the flush's dirty lines itself).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --next     # the widened paths: decode (Nq << Nk) and window
@@ -42,6 +44,24 @@ sys.path.insert(0, ROOT)
 from exact_io_aware_flashattention_gb300.inputs import BENCH_WORKLOAD, WORKLOADS, make_workload_inputs  # noqa: E402
 
 L2_FLUSH_BYTES = 256 * 2 ** 20
+L2_FLUSH_DESC = ("flushed between steps: 256 MiB write, then a 256 MiB read of another buffer so the write's "
+                 "dirty lines are written back before the step (all outside the timed events)")
+
+
+class L2Flush:
+    """Between timed steps: write a buffer larger than L2 (nothing of the
+    previous step stays resident), then read a second one, so that the lines
+    the write left dirty are written back here and not inside the next timed
+    step: the step starts from a cold and clean L2, the state ncu profiles
+    from."""
+
+    def __init__(self, torch, dev):
+        self.wr = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.wr.fill_(1)
+        self.rd.sum()
 FALLBACK_BF16_TFLOPS = 1900.0
 DOMINANT_KERNEL = "fa_bwd_dkdv_kernel"
 METRIC = "attention fwd/bwd TFLOPS (bf16, causal) and % of GB300 dense-bf16 peak, 1 GPU"
@@ -268,7 +288,7 @@ def run_reference(args, w):
 def workload_config(w):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
             "scale": w.scale, "global_batch": w.B, "seq_len": w.N,
-            "l2": "flushed between steps (256 MiB write outside the timed events)",
+            "l2": L2_FLUSH_DESC,
             "parallelism": "replicas (one independent workload per GPU)"}
 
 
@@ -301,7 +321,7 @@ def run_ours(args, w):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws_bytes = fa.fa_bwd_workspace_bytes(B, Hq, Hkv, N, d)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     ptr = lambda t: t.data_ptr()  # noqa: E731
@@ -329,7 +349,7 @@ def run_ours(args, w):
             ev[4].record(stream)
 
     for _ in range(max(3, args.warmup)):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize(dev)
     fa.check_device_status()
@@ -343,7 +363,7 @@ def run_ours(args, w):
     time.sleep(0.25)  # let the sampler attach before the timed region
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         step(events[i])
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -481,7 +501,7 @@ def _time_events(fn, steps, warmup, flush, stream):
         fn()
     total = 0.0
     for _ in range(steps):
-        flush.fill_(1)
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -500,7 +520,7 @@ def run_next(args):
     fa.load_library()
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     steps, warmup = max(args.steps, 20), max(args.warmup, 3)
     hbm, hbm_src = hbm_peak()
     peak, peak_src = bf16_peak()
@@ -533,7 +553,7 @@ def run_next(args):
         print(json.dumps({"case": "decode", "metric": "decode attention HBM throughput", "value": gbs,
                           "unit": "GB/s", "us": ms * 1e3, "dtype": "bf16", "data": "synthetic",
                           "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "Nq": Nq, "Nk": Nk, "d": d, "causal": True,
-                                     "num_splits": splits, "l2": "flushed before each run"},
+                                     "num_splits": splits, "l2": L2_FLUSH_DESC},
                           "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                                        "frac": gbs / hbm, "peak_source": hbm_src,
                                        "algorithmic_bytes": nbytes}}), flush=True)
@@ -570,7 +590,7 @@ def run_next(args):
                       "value": {"fwd": tf_f, "bwd": tf_b}, "unit": "TFLOPS",
                       "ms": {"fwd": ms_f, "bwd": ms_b}, "dtype": "bf16", "data": "synthetic",
                       "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "causal": True, "window": win,
-                                 "l2": "flushed before each run"},
+                                 "l2": L2_FLUSH_DESC},
                       "frac_of_peak": {"fwd": tf_f / peak, "bwd": tf_b / peak}, "peak_source": peak_src}),
           flush=True)
 
@@ -597,7 +617,7 @@ def run_next(args):
                       "value": {"deterministic": bf / (res[1] * 1e-3) / 1e12,
                                 "reduce_add": bf / (res[0] * 1e-3) / 1e12},
                       "unit": "TFLOPS", "ms": {"deterministic": res[1], "reduce_add": res[0]}, "dtype": "bf16",
-                      "data": "synthetic", "config": {"workload": w.name, "l2": "flushed before each run"}}),
+                      "data": "synthetic", "config": {"workload": w.name, "l2": L2_FLUSH_DESC}}),
           flush=True)
     return 0
 
