@@ -286,6 +286,7 @@ fa_status dkdv(const void* q, const void* k, const void* v, const void* dO, void
   a.causal = causal;
   a.window = window;
   a.with_dq = with_dq;
+  a.v8 = ((reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 31u) == 0;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_status(

@@ -530,14 +530,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bars->dkv_free);
           }
           if (key < N) {
+            uint32_t w[16];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint4 w;
-              w.x = cvt_bf16x2(__uint_as_float(v[c * 8 + 0]) * mul, __uint_as_float(v[c * 8 + 1]) * mul);
-              w.y = cvt_bf16x2(__uint_as_float(v[c * 8 + 2]) * mul, __uint_as_float(v[c * 8 + 3]) * mul);
-              w.z = cvt_bf16x2(__uint_as_float(v[c * 8 + 4]) * mul, __uint_as_float(v[c * 8 + 5]) * mul);
-              w.w = cvt_bf16x2(__uint_as_float(v[c * 8 + 6]) * mul, __uint_as_float(v[c * 8 + 7]) * mul);
-              *reinterpret_cast<uint4*>(dst + q * 32 + c * 8) = w;
+            for (int c = 0; c < 16; ++c)
+              w[c] = cvt_bf16x2(__uint_as_float(v[2 * c]) * mul, __uint_as_float(v[2 * c + 1]) * mul);
+            if (args.v8) {
+              // One row's 64 bytes in two 32-byte stores: a warp instruction
+              // writes whole 32-byte sectors of 32 rows.
+              st_global_v8(dst + q * 32, w);
+              st_global_v8(dst + q * 32 + 16, w + 8);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(dst + q * 32 + c * 8) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
             }
           }
         }

@@ -36,6 +36,7 @@ struct BwdArgs {
   int causal;
   int window;         // > 0: key j visible to query i only if j > i - window (with causal)
   int with_dq;        // 1: also add the dQ partials into dq_accum; 0: dK, dV only
+  int v8;             // dK and dV 32-byte aligned: their rows are written 32 bytes at a time
   float scale;        // softmax scale
   float scale_log2;   // scale * log2(e)
 };

@@ -127,6 +127,27 @@ def test_many_items_per_cta_ragged(cuda_lib, d, causal):
     assert_bwd(dq, dk, dv, rdq, rdk, rdv, f"many items d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_dkdv_outputs_only_16_byte_aligned(cuda_lib, d):
+    """dK / dV at addresses that are 16- but not 32-byte aligned (allowed by
+    the ABI) take the 16-byte store path and give the same bits."""
+    B, Hq, Hkv, N = 2, 4, 2, 384
+    q, k, v, do = (t.to(DEV) for t in make_qkvdo(B, Hq, Hkv, N, d, seed=77 + d))
+    scale = 1.0 / np.sqrt(d)
+    o, lse = fa.forward(q, k, v, causal=True, scale=scale)
+    _, dk_ref, dv_ref = fa.backward(q, k, v, o, lse, do, causal=True, scale=scale)
+    n = k.numel()
+    buf = torch.empty(2 * n + 64, dtype=torch.bfloat16, device=DEV)
+    assert buf.data_ptr() % 32 == 0
+    dk = buf[8:8 + n].view(k.shape)              # 16 bytes past a 32-byte boundary
+    dv = buf[n + 40:2 * n + 40].view(v.shape)
+    assert dk.data_ptr() % 32 == 16 and dv.data_ptr() % 32 == 16
+    fa.backward(q, k, v, o, lse, do, causal=True, scale=scale, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    assert torch.equal(dk, dk_ref) and torch.equal(dv, dv_ref)
+
+
 def test_gqa_equals_repeated_heads_on_gpu(cuda_lib):
     # Grouped attention == multi-head attention on K/V repeated per group.
     B, Hq, Hkv, N, d = 1, 8, 2, 640, 128
