@@ -57,7 +57,7 @@ class L2Flush:
 
     def __init__(self, torch, dev):
         self.wr = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        self.rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)   # sums without a cast
 
     def __call__(self):
         self.wr.fill_(1)
