@@ -305,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       __nv_bfloat16* dst =
           reinterpret_cast<__nv_bfloat16*>(args.dq) + (((size_t)b * args.Hq + h) * N + (size_t)q) * D + g * kHalfD;
+      // dQ rows start on 32-byte boundaries whenever dQ itself does.
+      const bool v8 = (reinterpret_cast<uintptr_t>(args.dq) & 31u) == 0;
 #pragma unroll
       for (int c = 0; c < kHalfD / 32; ++c) {
         uint32_t v[32];
@@ -312,14 +314,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence(v);
         if (q < N) {
+          uint32_t w[16];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 w;
-            w.x = cvt_bf16x2(__uint_as_float(v[u * 8 + 0]) * args.scale, __uint_as_float(v[u * 8 + 1]) * args.scale);
-            w.y = cvt_bf16x2(__uint_as_float(v[u * 8 + 2]) * args.scale, __uint_as_float(v[u * 8 + 3]) * args.scale);
-            w.z = cvt_bf16x2(__uint_as_float(v[u * 8 + 4]) * args.scale, __uint_as_float(v[u * 8 + 5]) * args.scale);
-            w.w = cvt_bf16x2(__uint_as_float(v[u * 8 + 6]) * args.scale, __uint_as_float(v[u * 8 + 7]) * args.scale);
-            *reinterpret_cast<uint4*>(dst + c * 32 + u * 8) = w;
+          for (int u = 0; u < 16; ++u)
+            w[u] = cvt_bf16x2(__uint_as_float(v[2 * u]) * args.scale, __uint_as_float(v[2 * u + 1]) * args.scale);
+          if (v8) {
+            // 32-byte stores: a warp instruction writes whole 32-byte sectors of 32 rows.
+            st_global_v8(dst + c * 32, w);
+            st_global_v8(dst + c * 32 + 16, w + 8);
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(dst + c * 32 + u * 8) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
           }
         }
       }

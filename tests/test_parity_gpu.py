@@ -148,6 +148,25 @@ def test_dkdv_outputs_only_16_byte_aligned(cuda_lib, d):
     assert torch.equal(dk, dk_ref) and torch.equal(dv, dv_ref)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_deterministic_dq_only_16_byte_aligned(cuda_lib, d):
+    """The deterministic dQ kernel writes a 16- (not 32-) byte aligned dQ through
+    its 16-byte store path, bit for bit as an aligned one."""
+    B, Hq, Hkv, N = 2, 4, 2, 384
+    q, k, v, do = (t.to(DEV) for t in make_qkvdo(B, Hq, Hkv, N, d, seed=99 + d))
+    scale = 1.0 / np.sqrt(d)
+    o, lse = fa.forward(q, k, v, causal=True, scale=scale)
+    dq_ref, _, _ = fa.backward(q, k, v, o, lse, do, causal=True, scale=scale, deterministic=True)
+    n = q.numel()
+    buf = torch.empty(n + 32, dtype=torch.bfloat16, device=DEV)
+    dq = buf[8:8 + n].view(q.shape)
+    assert dq.data_ptr() % 32 == 16
+    fa.backward(q, k, v, o, lse, do, causal=True, scale=scale, deterministic=True, dq=dq)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    assert torch.equal(dq, dq_ref)
+
+
 def test_gqa_equals_repeated_heads_on_gpu(cuda_lib):
     # Grouped attention == multi-head attention on K/V repeated per group.
     B, Hq, Hkv, N, d = 1, 8, 2, 640, 128
