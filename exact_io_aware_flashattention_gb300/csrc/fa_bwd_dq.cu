@@ -1,16 +1,24 @@
-// Deterministic dQ for the attention backward: one CTA per 128-row query tile
-// of one (head, batch) walks the key tiles the tile can see and accumulates
-// dQ = scale * sum_j dS_j K_j in tensor memory, in a fixed order, so dQ is
-// bitwise reproducible (the dK/dV kernel then runs without its dQ partials).
+// Deterministic dQ for the attention backward: persistent, one CTA per SM.
+// An item is one 128-row query tile of one (head, batch); the CTA walks the
+// key tiles the item can see and accumulates dQ = scale * sum_j dS_j K_j in
+// tensor memory, in a fixed order, so dQ is bitwise reproducible (the dK/dV
+// kernel then runs without its dQ partials).
 // It recomputes what the dK/dV kernel recomputes, from the saved LSE
 // ([FA-memory] "38.解释FlashAttention的显存优化原理", part 2(2); [QBank-36]
 // part 7), with queries instead of keys on the tensor-memory lanes:
 //   S = Q K_j^T, P = 2^(S * scale * log2 e - LSE * log2 e),
 //   dP = dO V_j^T, dS = P (dP - D), dQ += dS K_j.
 //
+// Items go heaviest first (the last query tile first under causal masking)
+// and are dealt to the CTAs in snake order.  The K / V rings, the two S
+// buffers and their barriers run on across items (a tile counter); the next
+// item's Q / dO are loaded as soon as the item's last dP MMA has completed,
+// while its last dS, dQ MMA and epilogue finish, and the next item's first dQ
+// MMA waits until the epilogue has read dQ out of tensor memory.
+//
 // CTA layout (320 threads):
-//   warp 0      TMA producer: Q, dO and the tile's 128 LSE / D values once,
-//               K and V per key tile (rings of kStages)
+//   warp 0      TMA producer: per item Q, dO and the item's 128 LSE / D
+//               values, K and V per key tile (rings of kStages)
 //   warp 1      TMEM allocator and MMA issuer
 //   warps 2-9   two compute warpgroups: thread t of a group owns query row t
 //               (TMEM lane t); group g handles key columns [64g, 64g+64) of S
@@ -19,7 +27,8 @@
 // written over each group's own first 32 columns of its S buffer and read
 // there by the dQ MMA.  Tensor pipe order: S_0 dP_0 | S_1 dP_1 dQ_0 | S_2 dP_2
 // dQ_1 ...  S_{j+2} reuses S buffer j % 2 once dQ_j has read dS_j from it;
-// dP_{j+1} waits until the compute threads have read dP_j.
+// dP_{j+1} waits until the compute threads have read dP_j.  An item's last
+// tile issues its own dQ right after its dP (S_0 dP_0 dQ_0 for one tile).
 #include "fa_internal.h"
 #include "sm103a.cuh"
 
@@ -47,7 +56,7 @@ struct DqSmem {
 
 enum : int {
   kSiteQ = 41, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteSFull, kSiteDpFull, kSiteDpFree,
-  kSiteDsFull, kSiteDqDone, kSiteDqFinal
+  kSiteDsFull, kSiteDqDone, kSiteDqFinal, kSiteQEmpty, kSiteLdFree, kSiteDqFree
 };
 
 struct Bars {
@@ -55,6 +64,9 @@ struct Bars {
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], ds_full[2], dq_done[2];
   uint64_t dp_full, dp_free, dq_final, drain;
+  uint64_t q_empty;   // the item's last dP MMA done: Q / dO may be replaced
+  uint64_t ld_free;   // every compute thread has read the item's LSE / D
+  uint64_t dq_free;   // the item's dQ read out of tensor memory
   uint32_t tmem_base;
   int abort;
 };
@@ -64,6 +76,34 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                    smem_u32(dst)),
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
+}
+
+// Item u: query tile nt - 1 - u / (Hq B) (heaviest first under causal
+// masking), then head fastest and batch, so the query heads of one kv group
+// run side by side on neighbouring CTAs and share K / V through L2.
+struct Item {
+  int h, b, i, jlo, n;
+};
+
+__device__ __forceinline__ Item decode_item(int u, const DqArgs& a, int nt) {
+  const int per = a.Hq * a.B;
+  const int t = u / per;
+  const int rem = u - t * per;
+  Item it;
+  it.h = rem % a.Hq;
+  it.b = rem / a.Hq;
+  it.i = nt - 1 - t;
+  // Key tiles [jlo, jlo + n) hold keys some row of the tile may see.
+  const int jhi = a.causal ? it.i + 1 : nt;
+  it.jlo = a.window > 0 ? max(0, it.i * kT - a.window + 1) / kT : 0;
+  it.n = jhi - it.jlo;
+  return it;
+}
+
+// The CTA's k-th item: rounds of gridDim.x items, alternating direction.
+__device__ __forceinline__ int item_of_round(int k) {
+  const int g = gridDim.x;
+  return k * g + ((k & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x);
 }
 
 template <int D>
@@ -87,14 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int N = args.N;
   const int nt = (N + kT - 1) / kT;
-  const int h = blockIdx.x;
-  const int b = blockIdx.y;
-  const int i = nt - 1 - (int)blockIdx.z;        // query tile (heaviest causal tiles launched first)
-  const int kvh = h / (args.Hq / args.Hkv);
-  // Key tiles [jlo, jhi) hold keys some row of this tile may see.
-  const int jhi = args.causal ? i + 1 : nt;
-  const int jlo = args.window > 0 ? max(0, i * kT - args.window + 1) / kT : 0;
-  const int n = jhi - jlo;
+  const int G = args.Hq / args.Hkv;
+  const int n_items = args.Hq * args.B * nt;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -113,6 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dp_free, 256);
     mbar_init(&bars->dq_final, 1);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->ld_free, 256);
+    mbar_init(&bars->dq_free, 256);
     bars->abort = 0;
     mbar_fence_init();
     fence_proxy_async_smem();
@@ -133,41 +170,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
   const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
   const int ntp = nt * kT;                       // padded rows per head of the LSE / D arrays
-  const size_t roff = ((size_t)b * args.Hq + h) * ntp + (size_t)i * kT;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bars->q_full, 2 * L::kTile + 1024u);
-      for (int a = 0; a < kAtoms; ++a) {
-        tma_load_4d(smem + L::kQ + a * kBlockBytes, &tmQ, &bars->q_full, a * 64, i * kT, h, b);
-        tma_load_4d(smem + L::kDO + a * kBlockBytes, &tmDO, &bars->q_full, a * 64, i * kT, h, b);
-      }
-      bulk_load(smem + L::kLse, args.lse2 + roff, 512u, &bars->q_full);
-      bulk_load(smem + L::kDr, args.drow + roff, 512u, &bars->q_full);
-      int issued = 0;
-      for (int jj = 0; jj < n; ++jj, ++issued) {
-        const int s = jj % SK, r = jj / SK;
-        if (r > 0 && !mbar_wait(&bars->k_empty[s], (r - 1) & 1, st, abort_flag, kSiteKEmpty)) break;
-        mbar_arrive_expect_tx(&bars->k_full[s], L::kTile);
-        for (int a = 0; a < kAtoms; ++a)
-          tma_load_4d(smem + L::kK + s * L::kTile + a * kBlockBytes, &tmK, &bars->k_full[s], a * 64,
-                      (jlo + jj) * kT, kvh, b);
-        if (r > 0 && !mbar_wait(&bars->v_empty[s], (r - 1) & 1, st, abort_flag, kSiteVEmpty)) {
-          ++issued;
-          break;
+      int nq = 0, nk = 0, nv = 0;                // Q / dO, K and V copies issued
+      bool pok = true;
+      for (int k = 0; pok; ++k) {
+        const int u = item_of_round(k);
+        if (u >= n_items) break;
+        const Item it = decode_item(u, args, nt);
+        // Q / dO and LSE / D of the previous item: its last dP MMA has
+        // completed and every compute thread has read its LSE / D.
+        if (nq > 0 && !mbar_wait(&bars->q_empty, (nq - 1) & 1, st, abort_flag, kSiteQEmpty)) break;
+        if (nq > 0 && !mbar_wait(&bars->ld_free, (nq - 1) & 1, st, abort_flag, kSiteLdFree)) break;
+        const size_t roff = ((size_t)it.b * args.Hq + it.h) * ntp + (size_t)it.i * kT;
+        mbar_arrive_expect_tx(&bars->q_full, 2 * L::kTile + 1024u);
+        for (int a = 0; a < kAtoms; ++a) {
+          tma_load_4d(smem + L::kQ + a * kBlockBytes, &tmQ, &bars->q_full, a * 64, it.i * kT, it.h, it.b);
+          tma_load_4d(smem + L::kDO + a * kBlockBytes, &tmDO, &bars->q_full, a * 64, it.i * kT, it.h, it.b);
         }
-        mbar_arrive_expect_tx(&bars->v_full[s], L::kTile);
-        for (int a = 0; a < kAtoms; ++a)
-          tma_load_4d(smem + L::kV + s * L::kTile + a * kBlockBytes, &tmV, &bars->v_full[s], a * 64,
-                      (jlo + jj) * kT, kvh, b);
+        bulk_load(smem + L::kLse, args.lse2 + roff, 512u, &bars->q_full);
+        bulk_load(smem + L::kDr, args.drow + roff, 512u, &bars->q_full);
+        ++nq;
+        const int kvh = it.h / G;
+        for (int jj = 0; jj < it.n; ++jj) {
+          const int s = nk % SK, r = nk / SK;
+          if (r > 0 && !mbar_wait(&bars->k_empty[s], (r - 1) & 1, st, abort_flag, kSiteKEmpty)) { pok = false; break; }
+          mbar_arrive_expect_tx(&bars->k_full[s], L::kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_4d(smem + L::kK + s * L::kTile + a * kBlockBytes, &tmK, &bars->k_full[s], a * 64,
+                        (it.jlo + jj) * kT, kvh, it.b);
+          ++nk;
+          if (r > 0 && !mbar_wait(&bars->v_empty[s], (r - 1) & 1, st, abort_flag, kSiteVEmpty)) { pok = false; break; }
+          mbar_arrive_expect_tx(&bars->v_full[s], L::kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_4d(smem + L::kV + s * L::kTile + a * kBlockBytes, &tmV, &bars->v_full[s], a * 64,
+                        (it.jlo + jj) * kT, kvh, it.b);
+          ++nv;
+        }
       }
-      // Every copy issued must have landed before the CTA may exit.
-      mbar_wait_drain(&bars->q_full, 0, st.timeout_ns);
-      for (int s = 0; s < SK && s < issued; ++s) {
-        const int last = issued - 1 - ((issued - 1 - s) % SK);
-        mbar_wait_drain(&bars->k_full[s], (last / SK) & 1, st.timeout_ns);
-        mbar_wait_drain(&bars->v_full[s], (last / SK) & 1, st.timeout_ns);
+      // Every copy issued must have landed before the CTA may exit: only the
+      // last copy into each buffer can still be in flight.
+      if (nq > 0) mbar_wait_drain(&bars->q_full, (nq - 1) & 1, st.timeout_ns);
+      for (int s = 0; s < SK; ++s) {
+        if (s < nk) mbar_wait_drain(&bars->k_full[s], ((nk - 1 - (nk - 1 - s) % SK) / SK) & 1, st.timeout_ns);
+        if (s < nv) mbar_wait_drain(&bars->v_full[s], ((nv - 1 - (nv - 1 - s) % SK) / SK) & 1, st.timeout_ns);
       }
     }
   } else if (warp == 1) {
@@ -179,11 +227,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQk = desc_kmajor(sQ, 0, kBlockBytes), dOk = desc_kmajor(sDO, 0, kBlockBytes);
       const uint64_t dKk = desc_kmajor(sK, 0, kBlockBytes), dKm = desc_mnmajor(sK, 0, kBlockBytes);
       const uint64_t dVk = desc_kmajor(sV, 0, kBlockBytes);
-      // dQ_j: A = dS_j in S buffer j % 2 (group g's keys at columns 64g..),
-      // B = K_j; releases the K stage afterwards.
-      auto issue_dq = [&](int jj) -> bool {
-        const int x = jj & 1, s = jj % SK;
-        if (!mbar_wait(&bars->ds_full[x], (jj >> 1) & 1, st, abort_flag, kSiteDsFull)) return false;
+      // dQ of tile tg (the item's jj-th, item ci): A = dS in S buffer tg % 2
+      // (group g's keys at columns 64g..), B = K; releases the K stage
+      // afterwards.  The item's first dQ overwrites the accumulator, so it
+      // waits until the previous item's dQ has been read out.
+      auto issue_dq = [&](int tg, int jj, int ci) -> bool {
+        const int x = tg & 1, s = tg % SK;
+        if (jj == 0 && ci > 0 && !mbar_wait(&bars->dq_free, (ci - 1) & 1, st, abort_flag, kSiteDqFree)) return false;
+        if (!mbar_wait(&bars->ds_full[x], (tg >> 1) & 1, st, abort_flag, kSiteDsFull)) return false;
         tc_fence_after();
         const uint64_t dk = dKm + (uint64_t)s * (L::kTile >> 4);
 #pragma unroll
@@ -194,34 +245,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars->k_empty[s]);
         return true;
       };
-      bool ok = mbar_wait(&bars->q_full, 0, st, abort_flag, kSiteQ);
-      for (int jj = 0; ok && jj < n; ++jj) {
-        const int x = jj & 1, s = jj % SK;
-        // S_jj overwrites dS_{jj-2} (read by dQ_{jj-2}).
-        if (jj >= 2 && !mbar_wait(&bars->dq_done[x], ((jj - 2) >> 1) & 1, st, abort_flag, kSiteDqDone)) break;
-        if (!mbar_wait(&bars->k_full[s], (jj / SK) & 1, st, abort_flag, kSiteKFull)) break;
-        tc_fence_after();
-        const uint64_t dk = dKk + (uint64_t)s * (L::kTile >> 4);
+      bool ok = true;
+      int tiles = 0;                             // tiles of the CTA's earlier items
+      for (int k = 0, ci = 0; ok; ++k, ++ci) {
+        const int u = item_of_round(k);
+        if (u >= n_items) break;
+        const int n = decode_item(u, args, nt).n;
+        if (!mbar_wait(&bars->q_full, ci & 1, st, abort_flag, kSiteQ)) break;
+        for (int jj = 0; jj < n; ++jj) {
+          const int tg = tiles + jj;
+          const int x = tg & 1, s = tg % SK;
+          // S_tg overwrites dS_{tg-2} (read by dQ_{tg-2}).
+          if (tg >= 2 && !mbar_wait(&bars->dq_done[x], ((tg - 2) >> 1) & 1, st, abort_flag, kSiteDqDone)) { ok = false; break; }
+          if (!mbar_wait(&bars->k_full[s], (tg / SK) & 1, st, abort_flag, kSiteKFull)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t dk = dKk + (uint64_t)s * (L::kTile >> 4);
 #pragma unroll
-        for (int k16 = 0; k16 < D / 16; ++k16)
-          mma_bf16_ss(tmem + x * 128, dQk + desc_step_kmajor(k16, kBlockBytes), dk + desc_step_kmajor(k16, kBlockBytes),
-                      idSS, k16 > 0);
-        mma_commit(&bars->s_full[x]);
-        // dP_jj overwrites dP_{jj-1}: the compute threads must have read it.
-        if (jj >= 1 && !mbar_wait(&bars->dp_free, (jj - 1) & 1, st, abort_flag, kSiteDpFree)) break;
-        if (!mbar_wait(&bars->v_full[s], (jj / SK) & 1, st, abort_flag, kSiteVFull)) break;
-        tc_fence_after();
-        const uint64_t dv = dVk + (uint64_t)s * (L::kTile >> 4);
+          for (int k16 = 0; k16 < D / 16; ++k16)
+            mma_bf16_ss(tmem + x * 128, dQk + desc_step_kmajor(k16, kBlockBytes),
+                        dk + desc_step_kmajor(k16, kBlockBytes), idSS, k16 > 0);
+          mma_commit(&bars->s_full[x]);
+          // dP_tg overwrites dP_{tg-1}: the compute threads must have read it.
+          if (tg >= 1 && !mbar_wait(&bars->dp_free, (tg - 1) & 1, st, abort_flag, kSiteDpFree)) { ok = false; break; }
+          if (!mbar_wait(&bars->v_full[s], (tg / SK) & 1, st, abort_flag, kSiteVFull)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t dv = dVk + (uint64_t)s * (L::kTile >> 4);
 #pragma unroll
-        for (int k16 = 0; k16 < D / 16; ++k16)
-          mma_bf16_ss(tDP, dOk + desc_step_kmajor(k16, kBlockBytes), dv + desc_step_kmajor(k16, kBlockBytes), idSS,
-                      k16 > 0);
-        mma_commit(&bars->dp_full);
-        mma_commit(&bars->v_empty[s]);
-        if (jj >= 1 && !issue_dq(jj - 1)) break;
-        if (jj == n - 1) ok = issue_dq(jj);
+          for (int k16 = 0; k16 < D / 16; ++k16)
+            mma_bf16_ss(tDP, dOk + desc_step_kmajor(k16, kBlockBytes), dv + desc_step_kmajor(k16, kBlockBytes),
+                        idSS, k16 > 0);
+          mma_commit(&bars->dp_full);
+          mma_commit(&bars->v_empty[s]);
+          if (jj == n - 1) mma_commit(&bars->q_empty);   // the item's Q / dO are no longer read
+          if (jj >= 1 && !issue_dq(tg - 1, jj - 1, ci)) { ok = false; break; }
+          if (jj == n - 1 && !issue_dq(tg, jj, ci)) { ok = false; break; }
+        }
+        if (!ok) break;
+        mma_commit(&bars->dq_final);
+        tiles += n;
       }
-      mma_commit(&bars->dq_final);
       mma_commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, st.timeout_ns);
     }
@@ -231,101 +293,115 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const int q = i * kT + r;                      // this thread's query
     const float sl2 = args.scale_log2;
     const uint64_t sl2x2 = f2pack(sl2, sl2);
-    bool ok = mbar_wait_warp(&bars->q_full, 0, st, abort_flag, kSiteQ);
-    // Rows past N have LSE*log2(e) = +inf in the padded array: P = 0.
-    const float lse2 = ok ? reinterpret_cast<const float*>(smem + L::kLse)[r] : 0.f;
-    const float drow = ok ? reinterpret_cast<const float*>(smem + L::kDr)[r] : 0.f;
-    const uint64_t nl2 = f2pack(-lse2, -lse2);
-    const uint64_t nd2 = f2pack(-drow, -drow);
-    for (int jj = 0; ok && jj < n; ++jj) {
-      const int x = jj & 1;
-      const int j = jlo + jj;
-      if (!mbar_wait_warp(&bars->s_full[x], (jj >> 1) & 1, st, abort_flag, kSiteSFull)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t tS = tmem + x * 128 + lane_off + g * 64;
-      uint32_t pr[2][32];
-      tmem_ld32(tS, pr[0]);
-      tmem_ld32(tS + 32, pr[1]);
-      tmem_wait_ld();
-      reg_fence(pr[0]);
-      reg_fence(pr[1]);
-      // Visible key columns of this group: [clo, chi) (causal: key <= q;
-      // window: key > q - w; keys past N never).
-      const int kc0 = j * kT + g * 64;             // key of the group's column 0
-      int chi = min(64, N - kc0);
-      if (args.causal) chi = min(chi, q + 1 - kc0);
-      const int clo = args.window > 0 ? max(0, q - args.window + 1 - kc0) : 0;
-#pragma unroll
-      for (int hq = 0; hq < 2; ++hq) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int col = hq * 32 + e;
-          float lo, hi;
-          f2unpack(ffma2(f2pack(__uint_as_float(pr[hq][e]), __uint_as_float(pr[hq][e + 1])), sl2x2, nl2), lo, hi);
-          lo = (col >= clo && col < chi) ? ex2(lo) : 0.f;
-          hi = (col + 1 >= clo && col + 1 < chi) ? ex2(hi) : 0.f;
-          pr[hq][e] = __float_as_uint(lo);
-          pr[hq][e + 1] = __float_as_uint(hi);
-        }
-      }
-      if (!mbar_wait_warp(&bars->dp_full, jj & 1, st, abort_flag, kSiteDpFull)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t dp[2][32];
-      tmem_ld32(tDP + lane_off + g * 64, dp[0]);
-      tmem_ld32(tDP + lane_off + g * 64 + 32, dp[1]);
-      tmem_wait_ld();
-      reg_fence(dp[0]);
-      reg_fence(dp[1]);
-      tc_fence_before();
-      mbar_arrive(&bars->dp_free);
-      uint32_t ds[32];
-#pragma unroll
-      for (int hq = 0; hq < 2; ++hq) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float a0, a1;
-          f2unpack(fmul2(f2pack(__uint_as_float(pr[hq][e]), __uint_as_float(pr[hq][e + 1])),
-                         fadd2(f2pack(__uint_as_float(dp[hq][e]), __uint_as_float(dp[hq][e + 1])), nd2)),
-                   a0, a1);
-          ds[hq * 16 + e / 2] = cvt_bf16x2(a0, a1);
-        }
-      }
-      // dS (bf16) over this group's own first 32 columns of the S buffer,
-      // already read into registers: the A operand of dQ_jj.
-      tmem_st32(tS, ds);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->ds_full[x]);
-    }
-
-    if (ok && mbar_wait_warp(&bars->dq_final, 0, st, abort_flag, kSiteDqFinal)) {
-      tc_fence_after();
-      __nv_bfloat16* dst =
-          reinterpret_cast<__nv_bfloat16*>(args.dq) + (((size_t)b * args.Hq + h) * N + (size_t)q) * D + g * kHalfD;
-      // dQ rows start on 32-byte boundaries whenever dQ itself does.
-      const bool v8 = (reinterpret_cast<uintptr_t>(args.dq) & 31u) == 0;
-#pragma unroll
-      for (int c = 0; c < kHalfD / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tDQ + lane_off + g * kHalfD + c * 32, v);
+    bool ok = true;
+    int tiles = 0;                                 // tiles of the CTA's earlier items
+    for (int k = 0, ci = 0; ok; ++k, ++ci) {
+      const int u = item_of_round(k);
+      if (u >= n_items) break;
+      const Item it = decode_item(u, args, nt);
+      const int q = it.i * kT + r;                 // this thread's query
+      if (!mbar_wait_warp(&bars->q_full, ci & 1, st, abort_flag, kSiteQ)) break;
+      // Rows past N have LSE*log2(e) = +inf in the padded array: P = 0.
+      const float lse2 = reinterpret_cast<const float*>(smem + L::kLse)[r];
+      const float drow = reinterpret_cast<const float*>(smem + L::kDr)[r];
+      mbar_arrive(&bars->ld_free);                 // the next item's LSE / D may replace them
+      const uint64_t nl2 = f2pack(-lse2, -lse2);
+      const uint64_t nd2 = f2pack(-drow, -drow);
+      for (int jj = 0; jj < it.n; ++jj) {
+        const int tg = tiles + jj;
+        const int x = tg & 1;
+        const int j = it.jlo + jj;
+        if (!mbar_wait_warp(&bars->s_full[x], (tg >> 1) & 1, st, abort_flag, kSiteSFull)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tS = tmem + x * 128 + lane_off + g * 64;
+        uint32_t pr[2][32];
+        tmem_ld32(tS, pr[0]);
+        tmem_ld32(tS + 32, pr[1]);
         tmem_wait_ld();
-        reg_fence(v);
-        if (q < N) {
+        reg_fence(pr[0]);
+        reg_fence(pr[1]);
+        // Visible key columns of this group: [clo, chi) (causal: key <= q;
+        // window: key > q - w; keys past N never).
+        const int kc0 = j * kT + g * 64;           // key of the group's column 0
+        int chi = min(64, N - kc0);
+        if (args.causal) chi = min(chi, q + 1 - kc0);
+        const int clo = args.window > 0 ? max(0, q - args.window + 1 - kc0) : 0;
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int col = hq * 32 + e;
+            float lo, hi;
+            f2unpack(ffma2(f2pack(__uint_as_float(pr[hq][e]), __uint_as_float(pr[hq][e + 1])), sl2x2, nl2), lo, hi);
+            lo = (col >= clo && col < chi) ? ex2(lo) : 0.f;
+            hi = (col + 1 >= clo && col + 1 < chi) ? ex2(hi) : 0.f;
+            pr[hq][e] = __float_as_uint(lo);
+            pr[hq][e + 1] = __float_as_uint(hi);
+          }
+        }
+        if (!mbar_wait_warp(&bars->dp_full, tg & 1, st, abort_flag, kSiteDpFull)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t dp[2][32];
+        tmem_ld32(tDP + lane_off + g * 64, dp[0]);
+        tmem_ld32(tDP + lane_off + g * 64 + 32, dp[1]);
+        tmem_wait_ld();
+        reg_fence(dp[0]);
+        reg_fence(dp[1]);
+        tc_fence_before();
+        mbar_arrive(&bars->dp_free);
+        uint32_t ds[32];
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float a0, a1;
+            f2unpack(fmul2(f2pack(__uint_as_float(pr[hq][e]), __uint_as_float(pr[hq][e + 1])),
+                           fadd2(f2pack(__uint_as_float(dp[hq][e]), __uint_as_float(dp[hq][e + 1])), nd2)),
+                     a0, a1);
+            ds[hq * 16 + e / 2] = cvt_bf16x2(a0, a1);
+          }
+        }
+        // dS (bf16) over this group's own first 32 columns of the S buffer,
+        // already read into registers: the A operand of dQ_jj.
+        tmem_st32(tS, ds);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->ds_full[x]);
+      }
+
+      if (!ok) break;
+      tiles += it.n;
+      if (!mbar_wait_warp(&bars->dq_final, ci & 1, st, abort_flag, kSiteDqFinal)) break;
+      tc_fence_after();
+      uint32_t v[kHalfD / 32][32];
+#pragma unroll
+      for (int c = 0; c < kHalfD / 32; ++c) tmem_ld32(tDQ + lane_off + g * kHalfD + c * 32, v[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < kHalfD / 32; ++c) reg_fence(v[c]);
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);                 // the next item's first dQ MMA may overwrite it
+      if (q < N) {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.dq) +
+                             (((size_t)it.b * args.Hq + it.h) * N + (size_t)q) * D + g * kHalfD;
+        // dQ rows start on 32-byte boundaries whenever dQ itself does.
+        const bool v8 = (reinterpret_cast<uintptr_t>(args.dq) & 31u) == 0;
+#pragma unroll
+        for (int c = 0; c < kHalfD / 32; ++c) {
           uint32_t w[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
-            w[u] = cvt_bf16x2(__uint_as_float(v[2 * u]) * args.scale, __uint_as_float(v[2 * u + 1]) * args.scale);
+          for (int e = 0; e < 16; ++e)
+            w[e] = cvt_bf16x2(__uint_as_float(v[c][2 * e]) * args.scale, __uint_as_float(v[c][2 * e + 1]) * args.scale);
           if (v8) {
             // 32-byte stores: a warp instruction writes whole 32-byte sectors of 32 rows.
             st_global_v8(dst + c * 32, w);
             st_global_v8(dst + c * 32 + 16, w + 8);
           } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              *reinterpret_cast<uint4*>(dst + c * 32 + u * 8) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<uint4*>(dst + c * 32 + e * 8) = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
           }
         }
       }
@@ -351,8 +427,15 @@ static cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, con
   static_assert(sizeof(Bars) <= 256, "barrier block");
   cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
-  const int nt = (a.N + kT - 1) / kT;
-  dim3 grid(a.Hq, a.B, nt);
+  // Persistent: one CTA per SM (the shared memory allows no second one),
+  // never more CTAs than items.
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long items = (long long)a.Hq * a.B * ((a.N + kT - 1) / kT);
+  const int grid = (int)(items < sms ? items : sms);
   fa_bwd_dq_kernel<D><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, a, st);
   return cudaGetLastError();
 }

@@ -109,6 +109,10 @@ def test_splits_agree_with_one_pass(cuda_lib):
     (1, 4, 4, 513, 128, False, 0),
     (1, 2, 2, 700, 64, True, 150),
     (1, 8, 2, 129, 128, True, 1),
+    # More query tiles than SMs: each persistent dQ CTA walks several items.
+    (4, 12, 4, 1000, 128, True, 0),
+    (4, 12, 12, 1000, 64, False, 0),
+    (3, 8, 2, 1100, 128, True, 200),
 ])
 def test_deterministic_backward(cuda_lib, B, Hq, Hkv, N, d, causal, window):
     q, k, v, do = make_qkvdo(B, Hq, Hkv, N, d, seed=N * 3 + d + window)
