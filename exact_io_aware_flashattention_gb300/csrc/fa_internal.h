@@ -51,7 +51,7 @@ struct DqArgs {
   float scale_log2;
 };
 
-// Deterministic dQ: one CTA per query tile, fixed accumulation order.
+// Deterministic dQ: persistent CTAs walking query-tile items, fixed accumulation order.
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, cudaStream_t stream);
 
