@@ -1,8 +1,11 @@
 #!/usr/bin/env python
 """Benchmark of the exact-attention hot path on GB300: one step = forward +
 backward (fa_fwd, then fa_bwd's three kernels) over one batch of synthetic
-bf16 inputs of the standard causal training shape (B=4, Hq=Hkv=16, N=2048,
-d=128).
+bf16 inputs of the long-context causal shape (B=1, Hq=Hkv=16, N=32768,
+d=128), the largest causal configuration; the standard causal (B4 H16 N2048),
+grouped-query causal (B2 Hq32 Hkv8 N8192), stressed non-causal d=64 and tiny
+workloads are timed the same way in the same run and reported under
+`per_config`.
 
 Prints ONE JSON line (rank 0).  `value` is TFLOPS under the convention
 fwd = 4*B*Hq*N^2*d (halved when causal), bwd = 2.5 x fwd, over the device time
@@ -12,6 +15,7 @@ a 256 MiB read of another buffer, so each step starts from a cold and clean
 L2 instead of writing back the flush's dirty lines itself).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-per-config] [--no-cpu-baseline]
   python bench.py --next     # the widened paths: decode (Nq << Nk) and window
 
 --next prints one JSON line per widened-path case (not the contract line):
@@ -109,6 +113,16 @@ def bf16_peak():
         return float(j["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
     except Exception:
         return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement)"
+
+
+def bf16_peak_sustained():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops_sustained"]), "measured (MEASURED_PEAKS.json bf16_tflops_sustained)"
+    except Exception:
+        return 1700.0, "fallback (1.7 PFLOP/s bf16 sustained, earlier GB300 measurement)"
 
 
 # Source files each timed kernel is compiled from; a committed ncu figure is
@@ -296,6 +310,93 @@ def workload_config(w):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+class Problem:
+    """Device buffers of one workload and one contract step over them: fa_fwd,
+    then fa_bwd's three kernels (preprocess, dK/dV, dQ conversion) through the
+    C ABI on one stream."""
+
+    def __init__(self, fa, torch, w, dev, stream):
+        self.fa, self.w, self.stream = fa, w, stream
+        self.host = make_workload_inputs(w)
+        self.q, self.k, self.v, self.do = (t.to(dev) for t in self.host)
+        B, Hq, Hkv, N, d = w.B, w.Hq, w.Hkv, w.N, w.d
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = torch.empty_like(self.q), torch.empty_like(self.k), torch.empty_like(self.v)
+        self.ws_bytes = fa.fa_bwd_workspace_bytes(B, Hq, Hkv, N, d)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+
+    def _call(self, status, what):
+        if status != 0:
+            raise self.fa.FAError(status, what)
+
+    def step(self, ev=None):
+        fa, w, sh = self.fa, self.w, self.stream.cuda_stream
+        B, Hq, Hkv, N, d = w.B, w.Hq, w.Hkv, w.N, w.d
+        p = lambda t: t.data_ptr()  # noqa: E731
+        if ev:
+            ev[0].record(self.stream)
+        self._call(fa.fa_fwd(p(self.q), p(self.k), p(self.v), p(self.o), p(self.lse), B, Hq, Hkv, N, d, w.causal,
+                             w.scale, sh), "fwd")
+        if ev:
+            ev[1].record(self.stream)
+        self._call(fa.fa_bwd_preprocess(p(self.o), p(self.do), p(self.lse), B, Hq, Hkv, N, d, p(self.ws),
+                                        self.ws_bytes, sh), "bwd_preprocess")
+        if ev:
+            ev[2].record(self.stream)
+        self._call(fa.fa_bwd_dkdv(p(self.q), p(self.k), p(self.v), p(self.do), p(self.dk), p(self.dv), B, Hq, Hkv,
+                                  N, d, w.causal, w.scale, p(self.ws), self.ws_bytes, sh), "bwd_dkdv")
+        if ev:
+            ev[3].record(self.stream)
+        self._call(fa.fa_bwd_dq_convert(p(self.dq), B, Hq, Hkv, N, d, w.scale, p(self.ws), self.ws_bytes, sh),
+                   "bwd_dq_convert")
+        if ev:
+            ev[4].record(self.stream)
+
+    def time(self, torch, steps, warmup, flush):
+        """Per-kernel mean device ms over `steps` steps (L2 flushed before each,
+        outside the events): dict fwd, pre, dkdv, conv, step, plus the step total."""
+        for _ in range(max(3, warmup)):
+            flush()
+            self.step()
+        torch.cuda.synchronize()
+        self.fa.check_device_status()
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        for i in range(steps):
+            flush()
+            self.step(events[i])
+        torch.cuda.synchronize()
+        self.fa.check_device_status()
+        ms = {"fwd": [e[0].elapsed_time(e[1]) for e in events], "pre": [e[1].elapsed_time(e[2]) for e in events],
+              "dkdv": [e[2].elapsed_time(e[3]) for e in events], "conv": [e[3].elapsed_time(e[4]) for e in events],
+              "step": [e[0].elapsed_time(e[4]) for e in events]}
+        out = {k: statistics.mean(v) for k, v in ms.items()}
+        out["step_total"] = sum(ms["step"])
+        return out
+
+
+def kernel_figures(w, t, peak):
+    """fwd / bwd TFLOPS and fractions of `peak` from Problem.time's means."""
+    bwd_ms = t["pre"] + t["dkdv"] + t["conv"]
+    fwd_tf = w.fwd_flops / (t["fwd"] * 1e-3) / 1e12
+    bwd_tf = w.bwd_flops / (bwd_ms * 1e-3) / 1e12
+    dkdv_tf = w.bwd_flops / (t["dkdv"] * 1e-3) / 1e12
+    return {
+        "fwd": {"tflops": fwd_tf, "ms": t["fwd"], "frac_of_peak": fwd_tf / peak},
+        "bwd": {"tflops": bwd_tf, "ms": bwd_ms, "frac_of_peak": bwd_tf / peak, "ms_preprocess": t["pre"],
+                "ms_dkdv": t["dkdv"], "ms_dq_convert": t["conv"], "dkdv_tflops": dkdv_tf,
+                "dkdv_frac_of_peak": dkdv_tf / peak},
+        "step": {"ms": t["step"], "tflops": (w.fwd_flops + w.bwd_flops) / (t["step"] * 1e-3) / 1e12},
+    }
+
+
+# The other workloads of the path, timed in the same run as the headline (one
+# line, `per_config`): the tiny and stressed ones are reported, the causal ones
+# carry the same targets as the headline.
+PER_CONFIG = ("tiny_b1_h1_n128_d64", "causal_b4_h16_n2048_d128", "gqa_causal_b2_hq32_hkv8_n8192_d128",
+              "stressed_b8_h32_n4096_d64")
+
+
 def run_ours(args, w):
     import torch
     import exact_io_aware_flashattention_gb300 as fa
@@ -313,44 +414,17 @@ def run_ours(args, w):
         dist.barrier()
     fa.load_library()
 
-    q_h, k_h, v_h, do_h = make_workload_inputs(w)
-    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
-    B, Hq, Hkv, N, d = w.B, w.Hq, w.Hkv, w.N, w.d
-    o = torch.empty_like(q)
-    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws_bytes = fa.fa_bwd_workspace_bytes(B, Hq, Hkv, N, d)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
-    ptr = lambda t: t.data_ptr()  # noqa: E731
-
-    def call(status, what):
-        if status != 0:
-            raise fa.FAError(status, what)
-
-    def step(ev=None):
-        if ev:
-            ev[0].record(stream)
-        call(fa.fa_fwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, Hq, Hkv, N, d, w.causal, w.scale, sh), "fwd")
-        if ev:
-            ev[1].record(stream)
-        call(fa.fa_bwd_preprocess(ptr(o), ptr(do), ptr(lse), B, Hq, Hkv, N, d, ptr(ws), ws_bytes, sh),
-             "bwd_preprocess")
-        if ev:
-            ev[2].record(stream)
-        call(fa.fa_bwd_dkdv(ptr(q), ptr(k), ptr(v), ptr(do), ptr(dk), ptr(dv), B, Hq, Hkv, N, d,
-                            w.causal, w.scale, ptr(ws), ws_bytes, sh), "bwd_dkdv")
-        if ev:
-            ev[3].record(stream)
-        call(fa.fa_bwd_dq_convert(ptr(dq), B, Hq, Hkv, N, d, w.scale, ptr(ws), ws_bytes, sh), "bwd_dq_convert")
-        if ev:
-            ev[4].record(stream)
+    flush = L2Flush(torch, dev)
+    prob = Problem(fa, torch, w, dev, stream)
+    q_h, k_h, v_h, do_h = prob.host
+    B, Hq, N = w.B, w.Hq, w.N
+    peak, peak_src = bf16_peak()
+    peak_sus, peak_sus_src = bf16_peak_sustained()
 
     for _ in range(max(3, args.warmup)):
         flush()
-        step()
+        prob.step()
     torch.cuda.synchronize(dev)
     fa.check_device_status()
 
@@ -364,7 +438,7 @@ def run_ours(args, w):
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush()
-        step(events[i])
+        prob.step(events[i])
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
@@ -372,39 +446,32 @@ def run_ours(args, w):
         dist.barrier()
     fa.check_device_status()
 
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in events]
-    pre_ms = [e[1].elapsed_time(e[2]) for e in events]
-    dkdv_ms = [e[2].elapsed_time(e[3]) for e in events]
-    conv_ms = [e[3].elapsed_time(e[4]) for e in events]
-    step_ms = [e[0].elapsed_time(e[4]) for e in events]
-    total_ms = max_over_ranks(sum(step_ms), dev)
+    t = {"fwd": statistics.mean(e[0].elapsed_time(e[1]) for e in events),
+         "pre": statistics.mean(e[1].elapsed_time(e[2]) for e in events),
+         "dkdv": statistics.mean(e[2].elapsed_time(e[3]) for e in events),
+         "conv": statistics.mean(e[3].elapsed_time(e[4]) for e in events),
+         "step": statistics.mean(e[0].elapsed_time(e[4]) for e in events)}
+    total_ms = max_over_ranks(sum(e[0].elapsed_time(e[4]) for e in events), dev)
     ms_per_step = total_ms / args.steps
     step_flops = w.fwd_flops + w.bwd_flops
     value = aggregate_tflops(step_flops, world, total_ms, args.steps)
-
-    peak, peak_src = bf16_peak()
-    fwd_avg = statistics.mean(fwd_ms)
-    bwd_avg = statistics.mean(p + k_ + c for p, k_, c in zip(pre_ms, dkdv_ms, conv_ms))
-    dkdv_avg = statistics.mean(dkdv_ms)
-    fwd_tflops = w.fwd_flops / (fwd_avg * 1e-3) / 1e12
-    bwd_tflops = w.bwd_flops / (bwd_avg * 1e-3) / 1e12
-    dkdv_tflops = w.bwd_flops / (dkdv_avg * 1e-3) / 1e12
-    if dkdv_avg >= fwd_avg:
-        dom, dom_flops, dom_ms = "fa_bwd_dkdv_kernel", w.bwd_flops, dkdv_avg
+    figs = kernel_figures(w, t, peak)
+    if t["dkdv"] >= t["fwd"]:
+        dom, dom_flops, dom_ms = "fa_bwd_dkdv_kernel", w.bwd_flops, t["dkdv"]
     else:
-        dom, dom_flops, dom_ms = "fa_fwd_kernel", w.fwd_flops, fwd_avg
+        dom, dom_flops, dom_ms = "fa_fwd_kernel", w.fwd_flops, t["fwd"]
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     src_hash = {k: kernel_source_hash(k) for k in KERNEL_SOURCES}
 
     # ---------------- e2e through host buffers (pinned), copies inside the timed region
     e2e = None
     if rank == 0 or world > 1:
-        pin = lambda t: t.pin_memory()  # noqa: E731
+        pin = lambda t_: t_.pin_memory()  # noqa: E731
         hq, hk, hv, hdo = pin(q_h), pin(k_h), pin(v_h), pin(do_h)
         ho, hlse = pin(torch.empty_like(q_h)), pin(torch.empty((B, Hq, N), dtype=torch.float32))
         hdq, hdk, hdv = pin(torch.empty_like(q_h)), pin(torch.empty_like(k_h)), pin(torch.empty_like(v_h))
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-        d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+        d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
 
         # Steps are pipelined the way a training loop prefetches: step i's
         # inputs are copied in on one stream while step i-1 computes, and its
@@ -412,8 +479,9 @@ def run_ours(args, w):
         # device buffer sets alternate; each step still moves all of its
         # inputs in and all of its outputs (O, LSE, dQ, dK, dV) out inside
         # the timed region.
-        sets = [dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv, ws=ws)]
-        sets.append({name: torch.empty_like(t) for name, t in sets[0].items()})
+        sets = [dict(q=prob.q, k=prob.k, v=prob.v, do=prob.do, o=prob.o, lse=prob.lse, dq=prob.dq, dk=prob.dk,
+                     dv=prob.dv, ws=prob.ws)]
+        sets.append({name: torch.empty_like(x) for name, x in sets[0].items()})
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev_in = [torch.cuda.Event() for _ in range(2)]
         ev_c = [torch.cuda.Event() for _ in range(2)]
@@ -461,6 +529,25 @@ def run_ours(args, w):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": n_e2e, "path": "pinned host -> fa.forward/fa.backward (C ABI) -> pinned host, "
                "copies on their own streams, overlapping the neighbouring steps' compute"}
+        del sets, hq, hk, hv, hdo, ho, hlse, hdq, hdk, hdv
+
+    # ---------------- the other workloads, same run, same step, same timing
+    per_config = None
+    if rank == 0 and not args.no_per_config:
+        per_config = {}
+        pc_sampler = ClockSampler(getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None))
+        pc_sampler.start()
+        for name in PER_CONFIG:
+            if name == w.name:
+                continue
+            pw = WORKLOADS[name]
+            pp = Problem(fa, torch, pw, dev, stream)
+            pt = pp.time(torch, args.per_config_steps, 3, flush)
+            per_config[name] = kernel_figures(pw, pt, peak)
+            del pp
+            torch.cuda.empty_cache()
+        per_config["clocks"] = pc_sampler.stop()
+        per_config["steps"] = args.per_config_steps
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -472,14 +559,15 @@ def run_ours(args, w):
             "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(w),
-            "fwd": {"tflops": fwd_tflops, "ms": fwd_avg, "frac_of_peak": fwd_tflops / peak},
-            "bwd": {"tflops": bwd_tflops, "ms": bwd_avg, "frac_of_peak": bwd_tflops / peak,
-                    "ms_preprocess": statistics.mean(pre_ms), "ms_dkdv": dkdv_avg,
-                    "ms_dq_convert": statistics.mean(conv_ms)},
+            "fwd": figs["fwd"],
+            "bwd": figs["bwd"],
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
+                         "frac_of_sustained": achieved / peak_sus, "sustained_peak": peak_sus,
+                         "sustained_peak_source": peak_sus_src,
                          "traffic": ncu_traffic(dom, w.name),
                          "algorithmic_flops_per_launch": dom_flops},
+            "per_config": per_config,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks,
@@ -596,7 +684,7 @@ def run_next(args):
 
     # Deterministic backward (separate dQ kernel) on the standard causal
     # workload, against the reduce-add backward.
-    w = WORKLOADS[BENCH_WORKLOAD]
+    w = WORKLOADS["causal_b4_h16_n2048_d128"]
     B, Hq, Hkv, N, d = w.B, w.Hq, w.Hkv, w.N, w.d
     q, k, v, do = (t.to(dev) for t in make_workload_inputs(w))
     o, lse = fa.forward(q, k, v, causal=True, scale=w.scale)
@@ -625,11 +713,13 @@ def run_next(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="time the headline workload only")
+    ap.add_argument("--per-config-steps", type=int, default=20)
     ap.add_argument("--next", action="store_true", help="measure the widened paths (decode, window) instead")
     args = ap.parse_args()
     if args.next:

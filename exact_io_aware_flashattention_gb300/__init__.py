@@ -3,7 +3,9 @@
 The names ``fa_fwd``, ``fa_fwd_ex``, ``fa_fwd_ex_workspace_bytes``,
 ``fa_fwd_ex_default_splits``, ``fa_bwd``, ``fa_bwd_ex``, ``fa_bwd_preprocess``,
 ``fa_bwd_dkdv``, ``fa_bwd_dq_convert``, ``fa_bwd_workspace_bytes``, ``fa_strerror``,
-``fa_last_device_status``, ``fa_selftest_wait_timeout`` and ``fa_version`` are
+``fa_last_device_status``, ``fa_selftest_wait_timeout``,
+``fa_selftest_drain_timeout``, ``fa_bwd_noalloc``, ``fa_last_cuda_error`` and
+``fa_version`` are
 the C entry points of ``include/fa.h`` with the same arguments (pointers as
 Python ints, stream as an int handle); they return the integer status.
 
@@ -38,6 +40,7 @@ FA_ERR_CUDA = 9
 FA_ERR_BAD_ARGUMENT = 10
 FA_ERR_ALIASING = 11
 FA_ERR_SCRATCH_LIMIT = 12
+FA_ERR_DEVICE_DRAIN = 13
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
@@ -69,6 +72,7 @@ _SIGNATURES = {
     "fa_strerror": ([_i], ctypes.c_char_p),
     "fa_last_device_status": ([_p, ctypes.POINTER(ctypes.c_int)], _i),
     "fa_selftest_wait_timeout": ([ctypes.c_ulonglong, _p], _i),
+    "fa_selftest_drain_timeout": ([ctypes.c_ulonglong, _p], _i),
     "fa_version": ([], _i),
     "fa_last_cuda_error": ([], ctypes.c_char_p),
     "fa_bwd_noalloc": ([_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p], _i),
@@ -169,6 +173,10 @@ def fa_last_device_status(stream=None):
 
 def fa_selftest_wait_timeout(timeout_ns, stream=None):
     return load_library().fa_selftest_wait_timeout(int(timeout_ns), stream)
+
+
+def fa_selftest_drain_timeout(timeout_ns, stream=None):
+    return load_library().fa_selftest_drain_timeout(int(timeout_ns), stream)
 
 
 def fa_version():

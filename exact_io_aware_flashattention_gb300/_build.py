@@ -8,6 +8,7 @@ spills) is kept next to the library as ``ptxas.txt``.
 from __future__ import annotations
 
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -58,6 +59,36 @@ def _compile(src: str) -> tuple[str, str]:
     return obj, r.stderr + r.stdout
 
 
+# The forward kernel splits its launch allocation between warpgroups with
+# setmaxnreg; the split is only valid for this per-thread register count.
+FWD_KERNEL_REGS = 168
+
+
+def check_registers(ptxas_log: str) -> None:
+    """Fail the build if ptxas did not give every forward-kernel instance
+    exactly FWD_KERNEL_REGS registers (or spilled in it)."""
+    entry = None
+    seen = 0
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            entry = m.group(1)
+            continue
+        if entry and "fa_fwd_kernel" in entry:
+            m = re.search(r"Used (\d+) registers", line)
+            if m:
+                seen += 1
+                if int(m.group(1)) != FWD_KERNEL_REGS:
+                    raise RuntimeError(f"{entry}: ptxas used {m.group(1)} registers, the warpgroup register split "
+                                       f"needs exactly {FWD_KERNEL_REGS}")
+                entry = None
+            m = re.search(r"(\d+) bytes spill stores", line)
+            if m and int(m.group(1)) != 0:
+                raise RuntimeError(f"{entry}: {m.group(1)} bytes of register spills")
+    if seen == 0:
+        raise RuntimeError("ptxas reported no forward-kernel instance")
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile the library if any source is newer than it; return its path."""
     if not force and up_to_date():
@@ -69,6 +100,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with open(os.path.join(OUT_DIR, "ptxas.txt"), "w") as f:
         for (o, log), src in zip(results, SOURCES):
             f.write(f"==== {src}\n{log}\n")
+    check_registers(results[SOURCES.index("fa_fwd.cu")][1])
     tmp = LIB_PATH + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)

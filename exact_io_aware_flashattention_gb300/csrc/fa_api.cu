@@ -4,6 +4,7 @@
 #include "fa.h"
 
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -44,9 +45,18 @@ fa_status cuda_status(cudaError_t e) {
     if (_e != cudaSuccess) return cuda_status(_e);    \
   } while (0)
 
-// First device-side error: code, block, wait site, thread.  Read and cleared
-// by fa_last_device_status.
-__device__ int g_status_words[4];
+// First device-side error: code, block, wait site, thread, and the first
+// failed drain (site, block).  Read and cleared by fa_last_device_status.
+__device__ int g_status_words[fa::kStatusWords];
+
+// Named range around each public call, for timeline tools (a no-op unless a
+// tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 __global__ void wait_selftest_kernel(fa::DevStatus st) {
   __shared__ uint64_t bar;
@@ -63,10 +73,24 @@ __global__ void wait_selftest_kernel(fa::DevStatus st) {
   __syncthreads();
 }
 
+// The same with the drain wait a kernel does on its way out: nothing ever
+// completes `bar`, so the drain gives up and records its site (98).
+__global__ void drain_selftest_kernel(fa::DevStatus st) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    fa::mbar_init(&bar, 1);
+    fa::mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) fa::mbar_wait_drain(&bar, 0, st, 98);
+  __syncthreads();
+}
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
   bool ready = false;
+  bool unusable = false;   // a kernel's drain gave up: no further launches on this device
   int num_sms = 0;
   int* status = nullptr;
 };
@@ -84,12 +108,17 @@ unsigned long long default_timeout_ns() {
   return t;
 }
 
-fa_status device_state(DeviceState** out) {
+// Per-device state, set up once with the device current: its SM count, the
+// status words' address, the kernels' shared-memory attributes and the
+// forward kernel's register check.  With `launch`, a device on which a drain
+// has failed is refused.
+fa_status device_state(DeviceState** out, bool launch = true) {
   int dev = -1;
   FA_TRY_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& s = g_dev[dev];
+  if (launch && s.unusable) return FA_ERR_DEVICE_DRAIN;
   if (!s.ready) {
     int major = 0, minor = 0, sms = 0;
     FA_TRY_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
@@ -106,6 +135,10 @@ fa_status device_state(DeviceState** out) {
           q != cudaDriverEntryPointSuccess || fn == nullptr)
         return FA_ERR_CUDA;
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    {
+      const cudaError_t e = fa::configure_kernels();
+      if (e != cudaSuccess) return launch_status(e);
     }
     s.num_sms = sms;
     s.status = static_cast<int*>(p);
@@ -199,7 +232,46 @@ WsLayout ws_layout(int B, int Hq, int N, int d) {
   return w;
 }
 
-fa_status tmap_bf16(CUtensorMap* m, const void* base, int B, int H, int N, int d) {
+// Tensor maps are a pure function of (kind, base address, sizes): a small
+// per-thread cache saves re-encoding them when the same buffers come back.
+struct TmapKey {
+  const void* base;
+  int kind, B, H, N, d;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && kind == o.kind && B == o.B && H == o.H && N == o.N && d == o.d;
+  }
+};
+struct TmapSlot {
+  TmapKey key{nullptr, -1, 0, 0, 0, 0};
+  CUtensorMap map;
+};
+constexpr int kTmapSlots = 32;
+thread_local TmapSlot t_tmaps[kTmapSlots];
+
+int tmap_slot(const TmapKey& k) {
+  uint64_t h = reinterpret_cast<uintptr_t>(k.base) >> 8;
+  h = h * 0x9E3779B97F4A7C15ull + (uint64_t)k.kind;
+  h = h * 0x9E3779B97F4A7C15ull + (uint64_t)(uint32_t)k.N;
+  h = h * 0x9E3779B97F4A7C15ull + (uint64_t)(uint32_t)(k.B * 131 + k.H * 7 + k.d);
+  return (int)((h >> 40) % kTmapSlots);
+}
+
+template <typename Encode>
+fa_status cached_tmap(CUtensorMap* m, const TmapKey& key, Encode encode) {
+  TmapSlot& slot = t_tmaps[tmap_slot(key)];
+  if (slot.key == key) {
+    *m = slot.map;
+    return FA_OK;
+  }
+  const fa_status st = encode(m);
+  if (st == FA_OK) {
+    slot.key = key;
+    slot.map = *m;
+  }
+  return st;
+}
+
+fa_status tmap_bf16_encode(CUtensorMap* m, const void* base, int B, int H, int N, int d) {
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2, (cuuint64_t)H * N * d * 2};
   cuuint32_t box[4] = {64, 128, 1, 1};
@@ -212,7 +284,7 @@ fa_status tmap_bf16(CUtensorMap* m, const void* base, int B, int H, int N, int d
 
 // Q (or O) [B, Hq, Nq, d] viewed as {d, Hq*Nq, B}: a 128-row box may start at
 // any row of a batch (a tile of one head, or the rows of a group of heads).
-fa_status tmap_rows_bf16(CUtensorMap* m, const void* base, int B, int H, int N, int d) {
+fa_status tmap_rows_bf16_encode(CUtensorMap* m, const void* base, int B, int H, int N, int d) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H * N, (cuuint64_t)B};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * N * d * 2};
   cuuint32_t box[3] = {64, 128, 1};
@@ -225,7 +297,7 @@ fa_status tmap_rows_bf16(CUtensorMap* m, const void* base, int B, int H, int N, 
 
 // fp32 dQ accumulator [B*Hq, N, d] viewed as {d, N, B*Hq} with a {32, 128, 1}
 // box and 128-byte swizzle, the target of the tiled TMA reduce-add.
-fa_status tmap_dq_accum(CUtensorMap* m, void* base, int B, int Hq, int N, int d) {
+fa_status tmap_dq_accum_encode(CUtensorMap* m, void* base, int B, int Hq, int N, int d) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)B * Hq};
   cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
   cuuint32_t box[3] = {32, 128, 1};
@@ -236,8 +308,19 @@ fa_status tmap_dq_accum(CUtensorMap* m, void* base, int B, int Hq, int N, int d)
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_LAUNCH;
 }
 
-
-
+// [B, H, N, d] bf16 as {d, N, H, B}, {64, 128, 1, 1} boxes.
+fa_status tmap_bf16(CUtensorMap* m, const void* base, int B, int H, int N, int d) {
+  return cached_tmap(m, TmapKey{base, 0, B, H, N, d},
+                     [&](CUtensorMap* x) { return tmap_bf16_encode(x, base, B, H, N, d); });
+}
+fa_status tmap_rows_bf16(CUtensorMap* m, const void* base, int B, int H, int N, int d) {
+  return cached_tmap(m, TmapKey{base, 1, B, H, N, d},
+                     [&](CUtensorMap* x) { return tmap_rows_bf16_encode(x, base, B, H, N, d); });
+}
+fa_status tmap_dq_accum(CUtensorMap* m, void* base, int B, int Hq, int N, int d) {
+  return cached_tmap(m, TmapKey{base, 2, B, Hq, N, d},
+                     [&](CUtensorMap* x) { return tmap_dq_accum_encode(x, base, B, Hq, N, d); });
+}
 
 fa_status validate_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B,
                         int Hq, int Hkv, int N, int d, int causal, float scale, const void* workspace,
@@ -297,7 +380,7 @@ fa_status dkdv(const void* q, const void* k, const void* v, const void* dO, void
 
 extern "C" {
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 101; }
 
 const char* fa_last_cuda_error(void) { return cudaGetErrorString(t_last_cuda_error); }
 
@@ -319,6 +402,9 @@ const char* fa_strerror(fa_status s) {
     case FA_ERR_ALIASING: return "an output overlaps an input or another output";
     case FA_ERR_SCRATCH_LIMIT:
       return "problem needs more scratch than fa_bwd_noalloc's built-in buffer (FA_NOALLOC_SCRATCH_BYTES) holds";
+    case FA_ERR_DEVICE_DRAIN:
+      return "a kernel exited with its own copies or MMAs possibly in flight after a device-side timeout; "
+             "no further launches on this device in this process";
   }
   return "unknown status";
 }
@@ -365,6 +451,7 @@ int fa_fwd_ex_default_splits(int B, int Hq, int Hkv, int Nq, int Nk, int d, int 
 fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
                     int Nk, int d, int causal, int window, int num_splits, float scale, void* workspace,
                     size_t workspace_bytes, void* stream) {
+  NvtxRange nv("fa_fwd_ex");
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_PTR;
   FA_TRY(check_shape_ex(B, Hq, Hkv, Nq, Nk, d));
   FA_TRY(check_scale(causal, scale));
@@ -424,6 +511,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
 
 fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, int B, int Hq, int Hkv, int N, int d,
                             void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nv("fa_bwd_preprocess");
   if (!o || !dO || !lse || !workspace) return FA_ERR_NULL_PTR;
   FA_TRY(check_shape(B, Hq, Hkv, N, d));
   if (!aligned16(o) || !aligned16(dO) || !aligned16(lse) || !aligned16(workspace)) return FA_ERR_MISALIGNED;
@@ -444,6 +532,7 @@ fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, int
 fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv, int B, int Hq,
                       int Hkv, int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
                       void* stream) {
+  NvtxRange nv("fa_bwd_dkdv");
   return dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, 0, 1, scale, workspace, workspace_bytes, stream);
 }
 
@@ -451,6 +540,7 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
 
 fa_status fa_bwd_dq_convert(void* dq, int B, int Hq, int Hkv, int N, int d, float scale, const void* workspace,
                             size_t workspace_bytes, void* stream) {
+  NvtxRange nv("fa_bwd_dq_convert");
   if (!dq || !workspace) return FA_ERR_NULL_PTR;
   FA_TRY(check_shape(B, Hq, Hkv, N, d));
   FA_TRY(check_scale(0, scale));
@@ -476,6 +566,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                     void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, int window,
                     int deterministic, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nv("fa_bwd_ex");
   if (!o || !dq || !lse) return FA_ERR_NULL_PTR;
   if (window < 0 || (window > 0 && !causal) || (deterministic != 0 && deterministic != 1)) return FA_ERR_BAD_ARGUMENT;
   FA_TRY(validate_dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
@@ -524,20 +615,32 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
   a.window = window;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_status(fa::launch_bwd_dq(d, tq, tk, tv, tdo, a, dev_status(ds), st));
+  return launch_status(fa::launch_bwd_dq(d, tq, tk, tv, tdo, a, dev_status(ds), ds->num_sms, st));
 }
 
 fa_status fa_last_device_status(void* stream, int* detail) {
-  {
-    const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_status(e);
-  }
+  NvtxRange nv("fa_last_device_status");
+  FA_TRY_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
   DeviceState* ds = nullptr;
-  FA_TRY(device_state(&ds));
-  int words[4] = {0, 0, 0, 0};
-  if (cudaMemcpy(words, ds->status, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
-  const int zero[4] = {0, 0, 0, 0};
-  if (cudaMemcpy(ds->status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  FA_TRY(device_state(&ds, false));
+  int words[fa::kStatusWords] = {};
+  FA_TRY_CUDA(cudaMemcpy(words, ds->status, sizeof(words), cudaMemcpyDeviceToHost));
+  const int zero[fa::kStatusWords] = {};
+  FA_TRY_CUDA(cudaMemcpy(ds->status, zero, sizeof(zero), cudaMemcpyHostToDevice));
+  if (words[4] != 0 || ds->unusable) {
+    // A block exited with copies or MMAs possibly still in flight: nothing
+    // more is launched on this device by this process.
+    {
+      std::lock_guard<std::mutex> lock(g_mu);
+      ds->unusable = true;
+    }
+    if (detail && words[4] != 0) {
+      detail[0] = words[5];
+      detail[1] = words[4];
+      detail[2] = -1;
+    }
+    return FA_ERR_DEVICE_DRAIN;
+  }
   if (detail) {
     detail[0] = words[1];
     detail[1] = words[2];
@@ -552,6 +655,15 @@ fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) 
   FA_TRY(device_state(&ds));
   fa::DevStatus st{ds->status, timeout_ns};
   wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st);
+  return launch_status(cudaGetLastError());
+}
+
+fa_status fa_selftest_drain_timeout(unsigned long long timeout_ns, void* stream) {
+  if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return FA_ERR_BAD_ARGUMENT;
+  DeviceState* ds = nullptr;
+  FA_TRY(device_state(&ds));
+  fa::DevStatus st{ds->status, timeout_ns};
+  drain_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st);
   return launch_status(cudaGetLastError());
 }
 
@@ -576,12 +688,13 @@ void* g_noalloc_ptr[kMaxDevices] = {};
 // device with that device current.
 fa_status noalloc_scratch(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  FA_TRY_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (g_noalloc_ptr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
+    FA_TRY_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    if (p == nullptr) return FA_ERR_CUDA;
     g_noalloc_ptr[dev] = p;
   }
   *out = g_noalloc_ptr[dev];
@@ -593,6 +706,7 @@ fa_status noalloc_scratch(void** out) {
 extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                                     const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
                                     int d, int causal, float scale, void* stream) {
+  NvtxRange nv("fa_bwd_noalloc");
   FA_TRY(check_shape(B, Hq, Hkv, N, d));
   if (ws_layout(B, Hq, N, d).total > (size_t)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL_PTR;

@@ -66,7 +66,9 @@ struct BwdSmem {
 
 enum : int {
   kSiteKV = 11, kSiteQEmpty, kSiteDoEmpty, kSiteLdEmpty, kSiteQFull, kSiteDvDone, kSiteDoFull, kSiteDqEmpty,
-  kSitePFull, kSiteDsFull, kSiteLdFull, kSiteSFull, kSiteDpFull, kSiteDqFull, kSiteDkvDone, kSiteStFull, kSiteDkDone
+  kSitePFull, kSiteDsFull, kSiteLdFull, kSiteSFull, kSiteDpFull, kSiteDqFull, kSiteDkvDone, kSiteStFull, kSiteDkDone,
+  // drains on the way out
+  kDrainKV = 31, kDrainLd, kDrainQ, kDrainDo, kDrainMma
 };
 
 struct Bars {
@@ -269,11 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         T += un.n_items;
       }
       // Every copy issued must have landed before the CTA may exit.
-      if (n_kv) mbar_wait_drain(&bars->kv_full, (n_kv - 1) & 1, st.timeout_ns);
+      if (n_kv) mbar_wait_drain(&bars->kv_full, (n_kv - 1) & 1, st, kDrainKV);
       for (int s = 0; s < 2; ++s) {
-        if (n_ld[s]) mbar_wait_drain(&bars->ld_full[s], (n_ld[s] - 1) & 1, st.timeout_ns);
-        if (n_q[s]) mbar_wait_drain(&bars->q_full[s], (n_q[s] - 1) & 1, st.timeout_ns);
-        if (n_do[s]) mbar_wait_drain(&bars->do_full[s], (n_do[s] - 1) & 1, st.timeout_ns);
+        if (n_ld[s]) mbar_wait_drain(&bars->ld_full[s], (n_ld[s] - 1) & 1, st, kDrainLd);
+        if (n_q[s]) mbar_wait_drain(&bars->q_full[s], (n_q[s] - 1) & 1, st, kDrainQ);
+        if (n_do[s]) mbar_wait_drain(&bars->do_full[s], (n_do[s] - 1) & 1, st, kDrainDo);
       }
     }
   } else if (warp == 1) {
@@ -361,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       T += un.n_items;
       }
       mma_commit(&bars->drain);
-      mbar_wait_drain(&bars->drain, 0, st.timeout_ns);
+      mbar_wait_drain(&bars->drain, 0, st, kDrainMma);
     }
   } else if (warp < 10) {
     // ------------------------------------------------------------ compute
@@ -690,15 +692,26 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float4* __
 }  // namespace
 
 template <int D, bool kDq>
+static cudaError_t configure_dkdv_d() {
+  using L = BwdSmem<D>;
+  static_assert(L::kBytes <= 232448, "shared memory budget");
+  static_assert(sizeof(Bars) <= 256, "barrier block");
+  return cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, kDq>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+}
+
+cudaError_t configure_bwd_kernels() {
+  cudaError_t e = configure_dkdv_d<64, true>();
+  if (e == cudaSuccess) e = configure_dkdv_d<64, false>();
+  if (e == cudaSuccess) e = configure_dkdv_d<128, true>();
+  if (e == cudaSuccess) e = configure_dkdv_d<128, false>();
+  return e;
+}
+
+template <int D, bool kDq>
 static cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, const DevStatus& st,
                                  int num_sms, cudaStream_t stream) {
   using L = BwdSmem<D>;
-  static_assert(L::kBytes <= 232448, "shared memory budget");
-  static_assert(sizeof(Bars) <= 256, "barrier block");
-  cudaError_t e =
-      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, kDq>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-  if (e != cudaSuccess) return e;
   const long long units = (long long)a.Hkv * a.B * ((a.N + kT - 1) / kT);
   const int grid = (int)(units < num_sms ? units : num_sms);
   fa_bwd_dkdv_kernel<D, kDq><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, a, st);

@@ -56,7 +56,9 @@ struct DqSmem {
 
 enum : int {
   kSiteQ = 41, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteSFull, kSiteDpFull, kSiteDpFree,
-  kSiteDsFull, kSiteDqDone, kSiteDqFinal, kSiteQEmpty, kSiteLdFree, kSiteDqFree
+  kSiteDsFull, kSiteDqDone, kSiteDqFinal, kSiteQEmpty, kSiteLdFree, kSiteDqFree,
+  // drains on the way out
+  kDrainQ = 61, kDrainK, kDrainV, kDrainMma
 };
 
 struct Bars {
@@ -212,10 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Every copy issued must have landed before the CTA may exit: only the
       // last copy into each buffer can still be in flight.
-      if (nq > 0) mbar_wait_drain(&bars->q_full, (nq - 1) & 1, st.timeout_ns);
+      if (nq > 0) mbar_wait_drain(&bars->q_full, (nq - 1) & 1, st, kDrainQ);
       for (int s = 0; s < SK; ++s) {
-        if (s < nk) mbar_wait_drain(&bars->k_full[s], ((nk - 1 - (nk - 1 - s) % SK) / SK) & 1, st.timeout_ns);
-        if (s < nv) mbar_wait_drain(&bars->v_full[s], ((nv - 1 - (nv - 1 - s) % SK) / SK) & 1, st.timeout_ns);
+        if (s < nk) mbar_wait_drain(&bars->k_full[s], ((nk - 1 - (nk - 1 - s) % SK) / SK) & 1, st, kDrainK);
+        if (s < nv) mbar_wait_drain(&bars->v_full[s], ((nv - 1 - (nv - 1 - s) % SK) / SK) & 1, st, kDrainV);
       }
     }
   } else if (warp == 1) {
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tiles += n;
       }
       mma_commit(&bars->drain);
-      mbar_wait_drain(&bars->drain, 0, st.timeout_ns);
+      mbar_wait_drain(&bars->drain, 0, st, kDrainMma);
     }
   } else {
     // ------------------------------------------------------------ compute
@@ -420,30 +422,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 template <int D>
-static cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, cudaStream_t stream) {
+static cudaError_t configure_dq_d() {
   using L = DqSmem<D>;
   static_assert(L::kBytes <= 232448, "shared memory budget");
   static_assert(sizeof(Bars) <= 256, "barrier block");
-  cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+}
+
+cudaError_t configure_dq_kernels() {
+  cudaError_t e = configure_dq_d<64>();
+  if (e == cudaSuccess) e = configure_dq_d<128>();
+  return e;
+}
+
+template <int D>
+static cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, int num_sms,
+                               cudaStream_t stream) {
+  using L = DqSmem<D>;
   // Persistent: one CTA per SM (the shared memory allows no second one),
   // never more CTAs than items.
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
   const long long items = (long long)a.Hq * a.B * ((a.N + kT - 1) / kT);
-  const int grid = (int)(items < sms ? items : sms);
+  const int grid = (int)(items < num_sms ? items : num_sms);
   fa_bwd_dq_kernel<D><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, a, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, cudaStream_t stream) {
-  if (d == 64) return launch_dq_d<64>(tq, tk, tv, tdo, a, st, stream);
-  return launch_dq_d<128>(tq, tk, tv, tdo, a, st, stream);
+                          const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, int num_sms,
+                          cudaStream_t stream) {
+  if (d == 64) return launch_dq_d<64>(tq, tk, tv, tdo, a, st, num_sms, stream);
+  return launch_dq_d<128>(tq, tk, tv, tdo, a, st, num_sms, stream);
 }
 
 }  // namespace fa

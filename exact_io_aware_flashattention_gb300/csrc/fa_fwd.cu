@@ -81,7 +81,9 @@ struct FwdCfg {
 // Wait-site ids reported in the status words.
 enum : int {
   kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSitePFull, kSiteVFull, kSiteOFree,
-  kSiteSFree, kSiteSFull, kSiteORescale, kSiteOLast, kSiteHand, kSiteLx, kSitePPrev, kSiteOStaged
+  kSiteSFree, kSiteSFull, kSiteORescale, kSiteOLast, kSiteHand, kSiteLx, kSitePPrev, kSiteOStaged,
+  // drains on the way out
+  kDrainQ = 21, kDrainK, kDrainV, kDrainS, kDrainPV
 };
 
 struct Bars {
@@ -333,10 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Every copy issued must have landed before the CTA may exit.
         for (int i = 0; i < 2; ++i)
-          if (q_issued[i]) mbar_wait_drain(&bars->q_full[i], (q_issued[i] - 1) & 1, st.timeout_ns);
+          if (q_issued[i]) mbar_wait_drain(&bars->q_full[i], (q_issued[i] - 1) & 1, st, kDrainQ);
         for (int s = 0; s < SK && s < kt; ++s) {
           const int last = kt - 1 - ((kt - 1 - s) % SK);   // last tile issued into stage s
-          mbar_wait_drain(&bars->k_full[s], (last / SK) & 1, st.timeout_ns);
+          mbar_wait_drain(&bars->k_full[s], (last / SK) & 1, st, kDrainK);
         }
       }
     } else if (warp == 2) {
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < SV && s < vt; ++s) {
           const int last = vt - 1 - ((vt - 1 - s) % SV);
-          mbar_wait_drain(&bars->v_full[s], (last / SV) & 1, st.timeout_ns);
+          mbar_wait_drain(&bars->v_full[s], (last / SV) & 1, st, kDrainV);
         }
       }
     } else if (warp == 1) {
@@ -391,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // No MMA may still be writing tensor memory when it is freed.
         mma_commit(&bars->drain_s);
-        mbar_wait_drain(&bars->drain_s, 0, st.timeout_ns);
+        mbar_wait_drain(&bars->drain_s, 0, st, kDrainS);
       }
     } else if (warp == 3) {
       // ------------------------------------------------------ P V issuer
@@ -416,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&bars->v_empty[v]);
         }
         mma_commit(&bars->drain_pv);
-        mbar_wait_drain(&bars->drain_pv, 0, st.timeout_ns);
+        mbar_wait_drain(&bars->drain_pv, 0, st, kDrainPV);
       }
     }
   } else {
@@ -665,6 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    // A wait that gave up between this tile's probability stores and their
+    // wait leaves them in flight: let them land before tensor memory is freed.
+    tmem_wait_st();
   }
 
   tc_fence_before();
@@ -679,9 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 template <int D, bool kGeneral>
-static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& to, const FwdArgs& a, const DevStatus& st, int num_sms,
-                                cudaStream_t stream) {
+static cudaError_t configure_fwd_d() {
   using L = FwdCfg<D>;
   static_assert(L::kBytes <= 232448, "shared memory budget");
   static_assert(sizeof(Bars) <= 512, "barrier block");
@@ -689,11 +692,28 @@ static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, co
       cudaFuncSetAttribute(fa_fwd_kernel<D, kGeneral>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   // The warpgroups' register shares assume this launch allocation; with any
-  // other, the softmax warpgroups' increase could never be granted.
+  // other, the softmax warpgroups' increase could never be granted.  The
+  // build checks the same count in ptxas's report; this guards a library
+  // built some other way.
   cudaFuncAttributes fattr;
   e = cudaFuncGetAttributes(&fattr, fa_fwd_kernel<D, kGeneral>);
   if (e != cudaSuccess) return e;
-  if (fattr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  return fattr.numRegs == kLaunchRegs ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
+cudaError_t configure_fwd_kernels() {
+  cudaError_t e = configure_fwd_d<64, false>();
+  if (e == cudaSuccess) e = configure_fwd_d<64, true>();
+  if (e == cudaSuccess) e = configure_fwd_d<128, false>();
+  if (e == cudaSuccess) e = configure_fwd_d<128, true>();
+  return e;
+}
+
+template <int D, bool kGeneral>
+static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& to, const FwdArgs& a, const DevStatus& st, int num_sms,
+                                cudaStream_t stream) {
+  using L = FwdCfg<D>;
   const long long items = (long long)a.nqt * a.splits * a.units;
   const int grid = (int)(items < num_sms ? items : num_sms);
   fa_fwd_kernel<D, kGeneral><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, to, a, st);

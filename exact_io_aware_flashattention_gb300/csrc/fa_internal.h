@@ -53,7 +53,8 @@ struct DqArgs {
 
 // Deterministic dQ: persistent CTAs walking query-tile items, fixed accumulation order.
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, cudaStream_t stream);
+                          const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, int num_sms,
+                          cudaStream_t stream);
 
 // `to` (O as a {d, N, Hq, B} bf16 map) is used by the plain self-attention
 // instance only.
@@ -74,6 +75,18 @@ cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
 cudaError_t launch_bwd_dq_convert(const float* dq_accum, void* dq, float scale, long long n, int num_sms,
                                   cudaStream_t stream);
 
-cudaError_t launch_wait_selftest(const DevStatus& st, cudaStream_t stream);
+// One-time set-up of the current device for each translation unit's kernels
+// (shared-memory sizes; the forward also checks that every instance was
+// compiled with the register count its warpgroup split assumes).
+cudaError_t configure_fwd_kernels();
+cudaError_t configure_bwd_kernels();
+cudaError_t configure_dq_kernels();
+
+inline cudaError_t configure_kernels() {
+  cudaError_t e = configure_fwd_kernels();
+  if (e == cudaSuccess) e = configure_bwd_kernels();
+  if (e == cudaSuccess) e = configure_dq_kernels();
+  return e;
+}
 
 }  // namespace fa

@@ -26,10 +26,16 @@ namespace fa {
 // ---------------------------------------------------------------------------
 // Device status words shared by all kernels of the library.
 //   [0] first error code (0 = none), [1] flattened block index,
-//   [2] wait-site id, [3] thread index.
+//   [2] wait-site id, [3] thread index,
+//   [4] wait-site id of the first failed drain (0 = none), [5] its block.
+// A drain is the wait, on a kernel's way out, for the TMA copies and MMAs it
+// has already issued; if one gives up, work may still be in flight when the
+// block exits, so the host treats the device as unusable from then on.
 // ---------------------------------------------------------------------------
+constexpr int kStatusWords = 8;
+
 struct DevStatus {
-  int* words;            // device pointer to 4 ints
+  int* words;            // device pointer to kStatusWords ints
   unsigned long long timeout_ns;
 };
 
@@ -120,13 +126,20 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, c
   return ok != 0;
 }
 
-// Bounded wait that ignores the abort flag (used to drain in-flight copies).
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, unsigned long long timeout_ns) {
+// Bounded wait that ignores the abort flag, used on a block's way out to let
+// the copies and MMAs it issued complete.  If it gives up, the site is
+// recorded in words [4] / [5] (the host then refuses further launches on the
+// device) and the block goes on to exit.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, const DevStatus& st, int site) {
   const uint32_t a = smem_u32(bar);
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((it & 63u) == 63u && globaltimer_ns() - t0 > timeout_ns) return false;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > st.timeout_ns) {
+      if (atomicCAS(st.words + 4, 0, site) == 0)
+        st.words[5] = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+      return false;
+    }
   }
 }
 

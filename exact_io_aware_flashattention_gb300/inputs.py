@@ -65,8 +65,9 @@ WORKLOADS = {
         "stressed_b8_h32_n4096_d64", 8, 32, 32, 4096, 64, False, 4, sigma_qk=3.0),
 }
 
-# The workload the benchmark reports on: the standard causal training shape.
-BENCH_WORKLOAD = "causal_b4_h16_n2048_d128"
+# The workload the benchmark reports on: the largest causal shape (B=1,
+# H=16, N=32768, d=128); the others are timed beside it in the same run.
+BENCH_WORKLOAD = "long_causal_b1_h16_n32768_d128"
 
 
 def make_qkvdo(B: int, Hq: int, Hkv: int, N: int, d: int, seed: int,

@@ -39,7 +39,8 @@
  *     calling thread (FA_ERR_UNSUPPORTED_DEVICE otherwise).
  *   - Every device-side wait is bounded: if a kernel's internal wait runs out
  *     (it should not), the kernel stops, leaves its outputs incomplete and
- *     records FA_ERR_DEVICE_TIMEOUT, which fa_last_device_status() reports.
+ *     records FA_ERR_DEVICE_TIMEOUT, which fa_last_device_status() reports
+ *     (see there for FA_ERR_DEVICE_DRAIN).
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -63,7 +64,10 @@ typedef enum fa_status {
   FA_ERR_CUDA = 9,                 /* another CUDA runtime error */
   FA_ERR_BAD_ARGUMENT = 10,        /* scale not finite / not > 0, causal not 0/1 */
   FA_ERR_ALIASING = 11,            /* an output overlaps an input or another output */
-  FA_ERR_SCRATCH_LIMIT = 12        /* fa_bwd_noalloc: problem needs more than FA_NOALLOC_SCRATCH_BYTES */
+  FA_ERR_SCRATCH_LIMIT = 12,       /* fa_bwd_noalloc: problem needs more than FA_NOALLOC_SCRATCH_BYTES */
+  FA_ERR_DEVICE_DRAIN = 13         /* after a device timeout a kernel exited with its own copies or MMAs
+                                      possibly still in flight: the library refuses further launches on
+                                      that device for the rest of the process */
 } fa_status;
 
 /*
@@ -190,6 +194,14 @@ const char* fa_strerror(fa_status status);
  * any kernel of this library recorded on the current device (FA_OK if none),
  * or FA_ERR_CUDA if the synchronisation itself failed.  If `detail` is not
  * NULL it receives 3 ints: flattened block index, wait-site id, thread index.
+ *
+ * A kernel whose bounded wait ran out stops its other roles and, on its way
+ * out, waits (bounded again) for the TMA copies and MMAs it had already
+ * issued before it frees its tensor memory.  If one of those drain waits also
+ * gives up, work of that block may still have been in flight when it exited;
+ * the call then returns FA_ERR_DEVICE_DRAIN (detail: block, drain site, -1)
+ * and from then on every entry point that would launch on this device
+ * returns FA_ERR_DEVICE_DRAIN without enqueuing anything.
  */
 fa_status fa_last_device_status(void* stream, int* detail);
 
@@ -200,6 +212,16 @@ fa_status fa_last_device_status(void* stream, int* detail);
  * FA_ERR_DEVICE_TIMEOUT and the device stays usable.  No fault is involved.
  */
 fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
+/*
+ * Self-test of the drain path: one CTA waits, the way a kernel does on its
+ * way out for the copies and MMAs it issued, on a barrier nothing completes,
+ * limited to `timeout_ns` (1e3 .. 1e10).  No copy or MMA is actually in
+ * flight and no fault is involved.  Afterwards fa_last_device_status()
+ * reports FA_ERR_DEVICE_DRAIN (site 98) and this process can launch nothing
+ * more on the device through this library: run it in a process of its own.
+ */
+fa_status fa_selftest_drain_timeout(unsigned long long timeout_ns, void* stream);
 
 /*
  * Backward pass for callers that must not allocate device memory.

@@ -52,3 +52,35 @@ def assert_bwd(dq, dk, dv, rdq, rdk, rdv, what=""):
         errs[name] = rel_l2(g, r)
         assert errs[name] <= GRAD_REL_L2, f"{what}: {name} rel-L2 {errs}"
     return errs
+
+
+class GuardedBuffers:
+    """Output buffers with guard bytes on both sides.
+
+    ``empty(shape, dtype)`` returns a contiguous CUDA view into a larger byte
+    buffer whose first and last GUARD bytes (and the view itself) are filled
+    with a fixed pattern; ``check()`` asserts that no guard byte changed, i.e.
+    that no kernel wrote outside the output it was given.  The views start
+    GUARD bytes into a fresh allocation, so they keep its 256-byte alignment.
+    """
+
+    GUARD = 4096
+    PATTERN = 0xA5
+
+    def __init__(self, device):
+        self.device = device
+        self.bufs = []
+
+    def empty(self, shape, dtype):
+        import torch
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        raw = torch.full((n + 2 * self.GUARD,), self.PATTERN, dtype=torch.uint8, device=self.device)
+        self.bufs.append((raw, n))
+        return raw[self.GUARD:self.GUARD + n].view(dtype).view(*shape)
+
+    def check(self):
+        for raw, n in self.bufs:
+            head = raw[:self.GUARD]
+            tail = raw[self.GUARD + n:]
+            assert bool((head == self.PATTERN).all()), "guard bytes before an output were overwritten"
+            assert bool((tail == self.PATTERN).all()), "guard bytes after an output were overwritten"

@@ -32,9 +32,10 @@ def test_binding_exposes_same_names():
 
 
 def test_version_and_strerror(lib):
-    assert fa.fa_version() == 100
-    for code in range(0, 13):
-        assert fa.fa_strerror(code)
+    assert fa.fa_version() == 101
+    for code in range(0, 14):
+        assert fa.fa_strerror(code) and fa.fa_strerror(code) != "unknown status"
+    assert "no further launches" in fa.fa_strerror(fa.FA_ERR_DEVICE_DRAIN)
     assert fa.fa_strerror(999) == "unknown status"
 
 

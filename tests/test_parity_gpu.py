@@ -237,3 +237,38 @@ def test_bounded_wait_reports_timeout_and_device_survives(cuda_lib):
     o, lse, *_ = run_gpu(q, k, v, do, False, 0.125)
     ro, rlse = ref.attention_forward(to_f64(q), to_f64(k), to_f64(v), False, 0.125)
     assert_fwd(o, lse, ro, rlse)
+
+
+def test_failed_drain_refuses_further_launches(cuda_lib):
+    """A drain wait that gives up (the self-test's barrier is never completed;
+    nothing is in flight and nothing faults) is reported as
+    FA_ERR_DEVICE_DRAIN, after which the library refuses every launch on the
+    device.  That state lasts for the process, so it runs in a child."""
+    import os
+    import subprocess
+    import sys
+    import textwrap
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = textwrap.dedent("""
+        import torch
+        import exact_io_aware_flashattention_gb300 as fa
+        fa.load_library()
+        s = torch.cuda.current_stream().cuda_stream
+        q = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")
+        o = torch.empty_like(q)
+        lse = torch.empty((1, 1, 128), dtype=torch.float32, device="cuda")
+        args = (q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 1, 1, 128, 64, 0, 0.125, s)
+        assert fa.fa_fwd(*args) == fa.FA_OK
+        assert fa.fa_last_device_status(s)[0] == fa.FA_OK
+        assert fa.fa_selftest_drain_timeout(2_000_000, s) == fa.FA_OK
+        st, detail = fa.fa_last_device_status(s)
+        assert st == fa.FA_ERR_DEVICE_DRAIN and detail[1] == 98, (st, detail)
+        assert fa.fa_fwd(*args) == fa.FA_ERR_DEVICE_DRAIN
+        assert fa.fa_selftest_wait_timeout(2_000_000, s) == fa.FA_ERR_DEVICE_DRAIN
+        assert fa.fa_last_device_status(s)[0] == fa.FA_ERR_DEVICE_DRAIN
+        torch.cuda.synchronize()          # the CUDA context itself is fine
+        print("drain refusal ok")
+    """)
+    env = dict(os.environ, PYTHONPATH=root + os.pathsep + os.environ.get("PYTHONPATH", ""))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "drain refusal ok" in r.stdout, r.stdout + r.stderr

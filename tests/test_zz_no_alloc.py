@@ -3,32 +3,35 @@ memory (for example code running under a memory manager that owns the whole
 device, or a plugin host that forbids cudaMalloc at run time).  Its scratch is
 a fixed buffer compiled into the library, so it takes no workspace argument.
 
-Checked through the C ABI against fa_bwd with a caller-owned workspace, on two
-calls in a row with different problems: the second call also shows that what
-the first call left in the shared buffer does not leak into its result.  This
-file is collected last so that a run stopping at the first failure has already
-run every other test.
+Checked through the C ABI on two calls in a row with different problems (the
+second call also shows that what the first call left in the shared buffer
+does not leak into its result): against the fp64 CPU oracle at the parity
+tolerance, and against fa_bwd with a caller-owned workspace.  The second
+problem uses a softmax scale away from 1/sqrt(d).  This file is collected
+last so that a run stopping at the first failure has already run every other
+test.
 """
 import pytest
 import torch
 
 import exact_io_aware_flashattention_gb300 as fa
-from exact_io_aware_flashattention_gb300.inputs import make_qkvdo
-from tests.parity import GRAD_REL_L2, as_f64, rel_l2
+from exact_io_aware_flashattention_gb300.inputs import make_qkvdo, to_f64
+from oracle import ref
+from tests.parity import GRAD_REL_L2, as_f64, assert_bwd, rel_l2
 
 pytestmark = pytest.mark.gpu
 
 PROBLEMS = [
-    # B, Hq, Hkv, N, d, causal, seed
-    (2, 4, 2, 1000, 128, True, 77),
-    (1, 6, 3, 777, 64, False, 78),
+    # B, Hq, Hkv, N, d, causal, scale, seed
+    (2, 4, 2, 1000, 128, True, 128 ** -0.5, 77),
+    (1, 6, 3, 777, 64, False, 0.3, 78),
 ]
 
 
-def _run_pair(B, Hq, Hkv, N, d, causal, seed):
+def _run_pair(B, Hq, Hkv, N, d, causal, scale, seed):
     assert fa.fa_bwd_workspace_bytes(B, Hq, Hkv, N, d) <= fa.NOALLOC_SCRATCH_BYTES
-    q, k, v, do = (t.cuda() for t in make_qkvdo(B, Hq, Hkv, N, d, seed=seed))
-    scale = d ** -0.5
+    qh, kh, vh, doh = make_qkvdo(B, Hq, Hkv, N, d, seed=seed)
+    q, k, v, do = (t.cuda() for t in (qh, kh, vh, doh))
     o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
     want = fa.backward(q, k, v, o, lse, do, causal=causal, scale=scale)   # existing entry point
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -44,12 +47,14 @@ def _run_pair(B, Hq, Hkv, N, d, causal, seed):
     free_after, _ = torch.cuda.mem_get_info()
     assert torch.cuda.memory_allocated() == allocated
     assert free_before - free_after < 2 * 2 ** 20
-    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), want):
-        err = rel_l2(as_f64(got), as_f64(ref))
+    rdq, rdk, rdv = ref.attention_backward(to_f64(qh), to_f64(kh), to_f64(vh), to_f64(doh), causal, scale)
+    assert_bwd(dq, dk, dv, rdq, rdk, rdv, f"fa_bwd_noalloc vs oracle, N={N} d={d} scale={scale:.3g}")
+    for name, got, other in zip(("dq", "dk", "dv"), (dq, dk, dv), want):
+        err = rel_l2(as_f64(got), as_f64(other))
         assert err <= GRAD_REL_L2, f"{name}: rel-L2 {err} vs fa_bwd"
 
 
-def test_noalloc_backward_matches_fa_bwd_on_two_calls(cuda_lib):
+def test_noalloc_backward_matches_oracle_and_fa_bwd_on_two_calls(cuda_lib):
     for problem in PROBLEMS:
         _run_pair(*problem)
 
