@@ -581,6 +581,33 @@ def run_ours(args, w):
     return 0
 
 
+def run_profile(args, w):
+    """A short launch sequence for profilers: `warmup` + `steps` contract steps
+    of the workload, no L2 flush, no timing, no host copies.  `--heads H`
+    scales the workload down to H query heads (and Hkv in proportion) so a
+    full counter capture stays small; traffic then scales with the heads."""
+    import dataclasses
+    import torch
+    import exact_io_aware_flashattention_gb300 as fa
+    from exact_io_aware_flashattention_gb300 import _build
+    _build.build()
+    fa.load_library()
+    if args.heads:
+        g = w.Hq // w.Hkv
+        if args.heads % g:
+            raise SystemExit(f"--heads must be a multiple of {g}")
+        w = dataclasses.replace(w, name=f"{w.name}@hq{args.heads}", Hq=args.heads, Hkv=args.heads // g)
+    dev = torch.device("cuda", 0)
+    prob = Problem(fa, torch, w, dev, torch.cuda.current_stream(dev))
+    for _ in range(args.warmup + args.steps):
+        prob.step()
+    torch.cuda.synchronize(dev)
+    fa.check_device_status()
+    print(json.dumps({"profile": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+                      "launches": 4 * (args.warmup + args.steps)}), flush=True)
+    return 0
+
+
 def _time_events(fn, steps, warmup, flush, stream):
     """Mean device ms of fn over `steps` runs (CUDA events on `stream`), with an
     L2 flush before each run outside the events."""
@@ -721,9 +748,14 @@ def main():
     ap.add_argument("--no-per-config", action="store_true", help="time the headline workload only")
     ap.add_argument("--per-config-steps", type=int, default=20)
     ap.add_argument("--next", action="store_true", help="measure the widened paths (decode, window) instead")
+    ap.add_argument("--profile", action="store_true",
+                    help="only run warmup + steps contract steps (for ncu); prints a short line, not the contract line")
+    ap.add_argument("--heads", type=int, default=0, help="with --profile: scale the workload to this many query heads")
     args = ap.parse_args()
     if args.next:
         return run_next(args)
+    if args.profile:
+        return run_profile(args, WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -243,7 +243,7 @@ struct TmapKey {
 };
 struct TmapSlot {
   TmapKey key{nullptr, -1, 0, 0, 0, 0};
-  CUtensorMap map;
+  CUtensorMap map;   // the encoded map of either rank
 };
 constexpr int kTmapSlots = 32;
 thread_local TmapSlot t_tmaps[kTmapSlots];
@@ -271,7 +271,7 @@ fa_status cached_tmap(CUtensorMap* m, const TmapKey& key, Encode encode) {
   return st;
 }
 
-fa_status tmap_bf16_encode(CUtensorMap* m, const void* base, int B, int H, int N, int d) {
+fa_status tmap_bf16_encode(CUtensorMap* m, const void* base, int B, int H, int N, int d) {  // rank 4
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2, (cuuint64_t)H * N * d * 2};
   cuuint32_t box[4] = {64, 128, 1, 1};
@@ -284,7 +284,7 @@ fa_status tmap_bf16_encode(CUtensorMap* m, const void* base, int B, int H, int N
 
 // Q (or O) [B, Hq, Nq, d] viewed as {d, Hq*Nq, B}: a 128-row box may start at
 // any row of a batch (a tile of one head, or the rows of a group of heads).
-fa_status tmap_rows_bf16_encode(CUtensorMap* m, const void* base, int B, int H, int N, int d) {
+fa_status tmap_rows_bf16_encode(CUtensorMap* m, const void* base, int B, int H, int N, int d) {  // rank 3
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H * N, (cuuint64_t)B};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * N * d * 2};
   cuuint32_t box[3] = {64, 128, 1};
@@ -297,7 +297,7 @@ fa_status tmap_rows_bf16_encode(CUtensorMap* m, const void* base, int B, int H, 
 
 // fp32 dQ accumulator [B*Hq, N, d] viewed as {d, N, B*Hq} with a {32, 128, 1}
 // box and 128-byte swizzle, the target of the tiled TMA reduce-add.
-fa_status tmap_dq_accum_encode(CUtensorMap* m, void* base, int B, int Hq, int N, int d) {
+fa_status tmap_dq_accum_encode(CUtensorMap* m, void* base, int B, int Hq, int N, int d) {  // rank 3
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)B * Hq};
   cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
   cuuint32_t box[3] = {32, 128, 1};
@@ -309,16 +309,16 @@ fa_status tmap_dq_accum_encode(CUtensorMap* m, void* base, int B, int Hq, int N,
 }
 
 // [B, H, N, d] bf16 as {d, N, H, B}, {64, 128, 1, 1} boxes.
-fa_status tmap_bf16(CUtensorMap* m, const void* base, int B, int H, int N, int d) {
-  return cached_tmap(m, TmapKey{base, 0, B, H, N, d},
+fa_status tmap_bf16(fa::TmaMap4* m, const void* base, int B, int H, int N, int d) {
+  return cached_tmap(&m->m, TmapKey{base, 0, B, H, N, d},
                      [&](CUtensorMap* x) { return tmap_bf16_encode(x, base, B, H, N, d); });
 }
-fa_status tmap_rows_bf16(CUtensorMap* m, const void* base, int B, int H, int N, int d) {
-  return cached_tmap(m, TmapKey{base, 1, B, H, N, d},
+fa_status tmap_rows_bf16(fa::TmaMap3* m, const void* base, int B, int H, int N, int d) {
+  return cached_tmap(&m->m, TmapKey{base, 1, B, H, N, d},
                      [&](CUtensorMap* x) { return tmap_rows_bf16_encode(x, base, B, H, N, d); });
 }
-fa_status tmap_dq_accum(CUtensorMap* m, void* base, int B, int Hq, int N, int d) {
-  return cached_tmap(m, TmapKey{base, 2, B, Hq, N, d},
+fa_status tmap_dq_accum(fa::TmaMap3* m, void* base, int B, int Hq, int N, int d) {
+  return cached_tmap(&m->m, TmapKey{base, 2, B, Hq, N, d},
                      [&](CUtensorMap* x) { return tmap_dq_accum_encode(x, base, B, Hq, N, d); });
 }
 
@@ -348,7 +348,8 @@ fa_status dkdv(const void* q, const void* k, const void* v, const void* dO, void
   FA_TRY(validate_dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, scale, workspace, workspace_bytes));
   DeviceState* ds = nullptr;
   FA_TRY(device_state(&ds));
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  fa::TmaMap4 tq, tk, tv, tdo;
+  fa::TmaMap3 tdq;
   const WsLayout w = ws_layout(B, Hq, N, d);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   FA_TRY(tmap_bf16(&tq, q, B, Hq, N, d));
@@ -480,7 +481,8 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
 
   DeviceState* ds = nullptr;
   FA_TRY(device_state(&ds));
-  CUtensorMap tq, tk, tv, to;
+  fa::TmaMap3 tq;
+  fa::TmaMap4 tk, tv, to;
   FA_TRY(tmap_rows_bf16(&tq, q, B, Hq, Nq, d));
   FA_TRY(tmap_bf16(&tk, k, B, Hkv, Nk, d));
   FA_TRY(tmap_bf16(&tv, v, B, Hkv, Nk, d));
@@ -598,7 +600,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
                                                  reinterpret_cast<float*>(ws + w.dr_off), nullptr, (long long)B * Hq,
                                                  N, ds->num_sms, st)));
   FA_TRY(dkdv(q, k, v, dO, dk, dv, B, Hq, Hkv, N, d, causal, window, 0, scale, workspace, workspace_bytes, stream));
-  CUtensorMap tq, tk, tv, tdo;
+  fa::TmaMap4 tq, tk, tv, tdo;
   FA_TRY(tmap_bf16(&tq, q, B, Hq, N, d));
   FA_TRY(tmap_bf16(&tk, k, B, Hkv, N, d));
   FA_TRY(tmap_bf16(&tv, v, B, Hkv, N, d));

@@ -120,9 +120,9 @@ __device__ __forceinline__ int unit_of_round(int k) {
 // reduce-adds; the store warp idles.
 template <int D, bool kDq>
 __global__ void __launch_bounds__(kThreads, 1)
-    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                       const __grid_constant__ CUtensorMap tmDQ, const BwdArgs args, const DevStatus st) {
+    fa_bwd_dkdv_kernel(const __grid_constant__ TmaMap4 tmQ, const __grid_constant__ TmaMap4 tmK,
+                       const __grid_constant__ TmaMap4 tmV, const __grid_constant__ TmaMap4 tmDO,
+                       const __grid_constant__ TmaMap3 tmDQ, const BwdArgs args, const DevStatus st) {
   using L = BwdSmem<D>;
   constexpr int kAtoms = D / 64;
   constexpr int kHalfD = D / 2;
@@ -708,8 +708,8 @@ cudaError_t configure_bwd_kernels() {
 }
 
 template <int D, bool kDq>
-static cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                 const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, const DevStatus& st,
+static cudaError_t launch_dkdv_d(const TmaMap4& tq, const TmaMap4& tk, const TmaMap4& tv,
+                                 const TmaMap4& tdo, const TmaMap3& tdq, const BwdArgs& a, const DevStatus& st,
                                  int num_sms, cudaStream_t stream) {
   using L = BwdSmem<D>;
   const long long units = (long long)a.Hkv * a.B * ((a.N + kT - 1) / kT);
@@ -718,8 +718,8 @@ static cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, const DevStatus& st,
+cudaError_t launch_bwd_dkdv(int d, const TmaMap4& tq, const TmaMap4& tk, const TmaMap4& tv,
+                            const TmaMap4& tdo, const TmaMap3& tdq, const BwdArgs& a, const DevStatus& st,
                             int num_sms, cudaStream_t stream) {
   if (a.with_dq) {
     if (d == 64) return launch_dkdv_d<64, true>(tq, tk, tv, tdo, tdq, a, st, num_sms, stream);

@@ -110,8 +110,8 @@ __device__ __forceinline__ int item_of_round(int k) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+    fa_bwd_dq_kernel(const __grid_constant__ TmaMap4 tmQ, const __grid_constant__ TmaMap4 tmK,
+                     const __grid_constant__ TmaMap4 tmV, const __grid_constant__ TmaMap4 tmDO,
                      const DqArgs args, const DevStatus st) {
   using L = DqSmem<D>;
   constexpr int kAtoms = D / 64;
@@ -436,8 +436,8 @@ cudaError_t configure_dq_kernels() {
 }
 
 template <int D>
-static cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, int num_sms,
+static cudaError_t launch_dq_d(const TmaMap4& tq, const TmaMap4& tk, const TmaMap4& tv,
+                               const TmaMap4& tdo, const DqArgs& a, const DevStatus& st, int num_sms,
                                cudaStream_t stream) {
   using L = DqSmem<D>;
   // Persistent: one CTA per SM (the shared memory allows no second one),
@@ -448,8 +448,8 @@ static cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, con
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, int num_sms,
+cudaError_t launch_bwd_dq(int d, const TmaMap4& tq, const TmaMap4& tk, const TmaMap4& tv,
+                          const TmaMap4& tdo, const DqArgs& a, const DevStatus& st, int num_sms,
                           cudaStream_t stream) {
   if (d == 64) return launch_dq_d<64>(tq, tk, tv, tdo, a, st, num_sms, stream);
   return launch_dq_d<128>(tq, tk, tv, tdo, a, st, num_sms, stream);

@@ -208,8 +208,8 @@ struct Cursor {
 
 template <int D, bool kGeneral>
 __global__ void __launch_bounds__(kThreads, 1)
-    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const FwdArgs args,
+    fa_fwd_kernel(const __grid_constant__ TmaMap3 tmQ, const __grid_constant__ TmaMap4 tmK,
+                  const __grid_constant__ TmaMap4 tmV, const __grid_constant__ TmaMap4 tmO, const FwdArgs args,
                   const DevStatus st) {
   using L = FwdCfg<D>;
   constexpr int kAtoms = D / 64;
@@ -710,8 +710,8 @@ cudaError_t configure_fwd_kernels() {
 }
 
 template <int D, bool kGeneral>
-static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& to, const FwdArgs& a, const DevStatus& st, int num_sms,
+static cudaError_t launch_fwd_d(const TmaMap3& tq, const TmaMap4& tk, const TmaMap4& tv,
+                                const TmaMap4& to, const FwdArgs& a, const DevStatus& st, int num_sms,
                                 cudaStream_t stream) {
   using L = FwdCfg<D>;
   const long long items = (long long)a.nqt * a.splits * a.units;
@@ -720,8 +720,8 @@ static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, co
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const FwdArgs& a, const DevStatus& st, int num_sms,
+cudaError_t launch_fwd(int d, const TmaMap3& tq, const TmaMap4& tk, const TmaMap4& tv,
+                       const TmaMap4& to, const FwdArgs& a, const DevStatus& st, int num_sms,
                        cudaStream_t stream) {
   const bool general = a.Nq != a.Nk || a.window > 0 || a.splits > 1 || a.packed;
   if (d == 64)

@@ -52,14 +52,14 @@ struct DqArgs {
 };
 
 // Deterministic dQ: persistent CTAs walking query-tile items, fixed accumulation order.
-cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const DqArgs& a, const DevStatus& st, int num_sms,
+cudaError_t launch_bwd_dq(int d, const TmaMap4& tq, const TmaMap4& tk, const TmaMap4& tv,
+                          const TmaMap4& tdo, const DqArgs& a, const DevStatus& st, int num_sms,
                           cudaStream_t stream);
 
-// `to` (O as a {d, N, Hq, B} bf16 map) is used by the plain self-attention
-// instance only.
-cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const FwdArgs& a, const DevStatus& st, int num_sms,
+// `tq` views Q as {d, Hq*Nq, B}; `to` (O as a {d, N, Hq, B} bf16 map) is
+// used by the plain self-attention instance only.
+cudaError_t launch_fwd(int d, const TmaMap3& tq, const TmaMap4& tk, const TmaMap4& tv,
+                       const TmaMap4& to, const FwdArgs& a, const DevStatus& st, int num_sms,
                        cudaStream_t stream);
 
 // (O, LSE) of several key splits -> O (bf16), LSE.
@@ -68,8 +68,8 @@ cudaError_t launch_fwd_merge(int d, const FwdArgs& a, int num_sms, cudaStream_t 
 cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dO, const float* lse, float* lse2, float* drow,
                                   float* dq_accum, long long heads, int N, int num_sms, cudaStream_t stream);
 
-cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, const DevStatus& st,
+cudaError_t launch_bwd_dkdv(int d, const TmaMap4& tq, const TmaMap4& tk, const TmaMap4& tv,
+                            const TmaMap4& tdo, const TmaMap3& tdq, const BwdArgs& a, const DevStatus& st,
                             int num_sms, cudaStream_t stream);
 
 cudaError_t launch_bwd_dq_convert(const float* dq_accum, void* dq, float scale, long long n, int num_sms,

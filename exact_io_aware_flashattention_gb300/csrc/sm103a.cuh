@@ -161,13 +161,25 @@ __device__ __forceinline__ void tc_fence_after() {
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+// A tensor map of rank R.  The rank is part of the type so that a tiled copy
+// instruction of one dimensionality can only be given a map encoded with the
+// same number of dimensions: a mismatch does not compile, instead of making
+// the copy unit fail at run time.
+template <int R>
+struct TmaMap {
+  CUtensorMap m;
+};
+using TmaMap3 = TmaMap<3>;
+using TmaMap4 = TmaMap<4>;
+
+template <int R>
+__device__ __forceinline__ void tma_prefetch_desc(const TmaMap<R>* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&m->m)) : "memory");
 }
 
 // 4-D tiled load {c0 = innermost, ...} into shared memory; completion is
 // reported as transaction bytes on *bar.
-__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1,
+__device__ __forceinline__ void tma_load_4d(void* dst, const TmaMap4* m, uint64_t* bar, int c0, int c1,
                                             int c2, int c3) {
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -176,7 +188,7 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1, int c2) {
+__device__ __forceinline__ void tma_load_3d(void* dst, const TmaMap3* m, uint64_t* bar, int c0, int c1, int c2) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
@@ -186,7 +198,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
 
 // Tiled 3-D reduce-add of a shared-memory box into global memory (the tensor
 // map's element type and reduction), tracked by this thread's bulk group.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t ssrc, int c0, int c1, int c2) {
+__device__ __forceinline__ void tma_reduce_add_3d(const TmaMap3* m, uint32_t ssrc, int c0, int c1, int c2) {
   asm volatile(
       "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
           reinterpret_cast<uint64_t>(m)),
@@ -196,7 +208,7 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t
 
 // Tiled 4-D store of a shared-memory box to global memory, tracked by this
 // thread's bulk group (rows outside the tensor are not written).
-__device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, uint32_t ssrc, int c0, int c1, int c2, int c3) {
+__device__ __forceinline__ void tma_store_4d(const TmaMap4* m, uint32_t ssrc, int c0, int c1, int c2, int c3) {
   asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
                    reinterpret_cast<uint64_t>(m)),
                "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(ssrc)
