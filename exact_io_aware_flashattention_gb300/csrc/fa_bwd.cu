@@ -89,9 +89,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 
 // A unit is one 128-key tile of one kv head of one batch; its CTA loops over
 // every query head of the group and every query tile that sees the key tile
-// (causal: i >= j; window w: i <= (128j + 126 + w) / 128).  Units go
+// (causal: i >= j; window w: i <= (128j + 126 + w) / 128).  Causal units go
 // heaviest first (smallest key tile first), dealt to the persistent CTAs in
-// snake order: rounds alternate direction over the CTAs.
+// snake order: rounds alternate direction over the CTAs.  Without causal
+// masking every unit costs the same and the key tiles of one kv head are
+// consecutive, so the units running at the same time share the query tiles
+// and the dQ accumulator rows of a few heads, which then stay in L2.
 struct Unit {
   int kvh, b, j, i0, nqi, n_items;
 };
@@ -99,8 +102,14 @@ struct Unit {
 __device__ __forceinline__ Unit decode_unit(int idx, const BwdArgs& a, int nt) {
   const int per = a.Hkv * a.B;
   Unit u;
-  u.j = idx / per;
-  const int kb = idx - u.j * per;
+  int kb;
+  if (a.causal) {
+    u.j = idx / per;
+    kb = idx - u.j * per;
+  } else {
+    kb = idx / nt;
+    u.j = idx - kb * nt;
+  }
   u.kvh = kb % a.Hkv;
   u.b = kb / a.Hkv;
   u.i0 = a.causal ? u.j : 0;
