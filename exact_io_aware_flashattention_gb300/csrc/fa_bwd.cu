@@ -92,23 +92,27 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // (causal: i >= j; window w: i <= (128j + 126 + w) / 128).  Causal units go
 // heaviest first (smallest key tile first), dealt to the persistent CTAs in
 // snake order: rounds alternate direction over the CTAs.  Without causal
-// masking every unit costs the same and the key tiles of one kv head are
-// consecutive, so the units running at the same time share the query tiles
-// and the dQ accumulator rows of a few heads, which then stay in L2.
+// masking every unit costs the same, and kHeadMajor puts the key tiles of one
+// kv head next to each other: the units running at the same time then share
+// the query tiles and dQ accumulator rows of a few heads, which stay in L2,
+// instead of touching every head's.  (A run-time switch between the two
+// orders slowed the causal kernel by 3-5 %, so the order is a compile-time
+// parameter.)
 struct Unit {
   int kvh, b, j, i0, nqi, n_items;
 };
 
+template <bool kHeadMajor>
 __device__ __forceinline__ Unit decode_unit(int idx, const BwdArgs& a, int nt) {
   const int per = a.Hkv * a.B;
   Unit u;
   int kb;
-  if (a.causal) {
-    u.j = idx / per;
-    kb = idx - u.j * per;
-  } else {
+  if constexpr (kHeadMajor) {
     kb = idx / nt;
     u.j = idx - kb * nt;
+  } else {
+    u.j = idx / per;
+    kb = idx - u.j * per;
   }
   u.kvh = kb % a.Hkv;
   u.b = kb / a.Hkv;
@@ -127,7 +131,7 @@ __device__ __forceinline__ int unit_of_round(int k) {
 // kDq = false: dK and dV only (the deterministic backward computes dQ in its
 // own kernel): no dQ MMA, no dS tile in shared memory, no dQ staging or
 // reduce-adds; the store warp idles.
-template <int D, bool kDq>
+template <int D, bool kDq, bool kHeadMajor>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ TmaMap4 tmQ, const __grid_constant__ TmaMap4 tmK,
                        const __grid_constant__ TmaMap4 tmV, const __grid_constant__ TmaMap4 tmDO,
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int round = 0; pok; ++round) {
         const int uidx = unit_of_round(round);
         if (uidx >= n_units) break;
-        const Unit un = decode_unit(uidx, args, nt);
+        const Unit un = decode_unit<kHeadMajor>(uidx, args, nt);
         // LSE*log2(e) and D of local item u (512 bytes each) go to slot
         // (T + u) % 2; they are issued one item ahead of that item's Q / dO.
         auto issue_ld = [&](int u) -> bool {
@@ -305,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int round = 0; ok; ++round, ++nu) {
         const int uidx = unit_of_round(round);
         if (uidx >= n_units) break;
-        const Unit un = decode_unit(uidx, args, nt);
+        const Unit un = decode_unit<kHeadMajor>(uidx, args, nt);
         if (!mbar_wait(&bars->kv_full, nu & 1, st, abort_flag, kSiteKV)) break;
       for (int t = 0; ok && t < un.n_items; ++t) {
         const int tg = T + t;
@@ -388,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int round = 0; ok; ++round, ++nu) {
     const int uidx = unit_of_round(round);
     if (uidx >= n_units) break;
-    const Unit un = decode_unit(uidx, args, nt);
+    const Unit un = decode_unit<kHeadMajor>(uidx, args, nt);
     const int key = un.j * kT + r;
     for (int t = 0; t < un.n_items; ++t) {
       const int tg = T + t;
@@ -574,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int round = 0; sok; ++round) {
       const int uidx = unit_of_round(round);
       if (uidx >= n_units) break;
-      const Unit un = decode_unit(uidx, args, nt);
+      const Unit un = decode_unit<kHeadMajor>(uidx, args, nt);
       for (int t = 0; t < un.n_items; ++t) {
         const int tg = T + t;
         const int slot = tg & 1;
@@ -705,7 +709,10 @@ static cudaError_t configure_dkdv_d() {
   using L = BwdSmem<D>;
   static_assert(L::kBytes <= 232448, "shared memory budget");
   static_assert(sizeof(Bars) <= 256, "barrier block");
-  return cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, kDq>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, kDq, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, kDq, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
 }
 
 cudaError_t configure_bwd_kernels() {
@@ -723,7 +730,10 @@ static cudaError_t launch_dkdv_d(const TmaMap4& tq, const TmaMap4& tk, const Tma
   using L = BwdSmem<D>;
   const long long units = (long long)a.Hkv * a.B * ((a.N + kT - 1) / kT);
   const int grid = (int)(units < num_sms ? units : num_sms);
-  fa_bwd_dkdv_kernel<D, kDq><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, a, st);
+  if (a.causal)
+    fa_bwd_dkdv_kernel<D, kDq, false><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, a, st);
+  else
+    fa_bwd_dkdv_kernel<D, kDq, true><<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, a, st);
   return cudaGetLastError();
 }
 

@@ -80,26 +80,17 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
-// Item u under causal masking: query tile nt - 1 - u / (Hq B) (heaviest
-// first), then head fastest and batch, so the query heads of one kv group run
-// side by side on neighbouring CTAs and share K / V through L2.  Without
-// causal masking every item costs the same and the query tiles of one head
-// are consecutive, so the CTAs running at the same time read the K / V of a
-// few heads only.
+// Item u: query tile nt - 1 - u / (Hq B) (heaviest first under causal
+// masking), then head fastest and batch, so the query heads of one kv group
+// run side by side on neighbouring CTAs and share K / V through L2.
 struct Item {
   int h, b, i, jlo, n;
 };
 
 __device__ __forceinline__ Item decode_item(int u, const DqArgs& a, int nt) {
   const int per = a.Hq * a.B;
-  int t, rem;
-  if (a.causal) {
-    t = u / per;
-    rem = u - t * per;
-  } else {
-    rem = u / nt;
-    t = u - rem * nt;
-  }
+  const int t = u / per;
+  const int rem = u - t * per;
   Item it;
   it.h = rem % a.Hq;
   it.b = rem / a.Hq;

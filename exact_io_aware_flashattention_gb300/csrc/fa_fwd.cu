@@ -72,9 +72,9 @@ struct FwdCfg {
   static constexpr uint32_t kQ = 0;                              // 2 slots
   static constexpr uint32_t kK = kQ + 2u * kTile;
   static constexpr uint32_t kV = kK + kStagesK * kTile;
-  static constexpr uint32_t kMref = kV + kStagesV * kTile;     // reference-max hand-off, 128 fp32
-  static constexpr uint32_t kLx = kMref + 512u;                // row-sum hand-off, 2 x 128 float2
-  static constexpr uint32_t kBar = kLx + 2048u;
+  static constexpr uint32_t kMref = kV + kStagesV * kTile;     // reference-max hand-off, 2 x 128 fp32
+  static constexpr uint32_t kLx = kMref + 1024u;               // row-sum hand-off, 2 x 128 fp32
+  static constexpr uint32_t kBar = kLx + 1024u;
   static constexpr uint32_t kBytes = kBar + 512u;
 };
 
@@ -115,28 +115,18 @@ struct Item {
 // A query tile is 128 consecutive query rows of one head, or, when packed,
 // the rows of all Hq/Hkv heads of one kv group (G * Nq <= 128 rows), so that
 // the group reads each K / V tile once.  Query row i stands at key position
-// i + Nk - Nq.  Causal work items are ordered heaviest first: rank r covers
-// query tile nqt-1-r of every unit, each split of it in turn.  Without causal
-// masking every item costs the same, so the items of one unit (head) are
-// consecutive instead: the CTAs working at the same time then stream the K /
-// V tiles of a few heads, which stay in L2, rather than those of every head.
-// An item may own no key tile (a split outside the tile's visible range);
-// every role skips such items.
+// i + Nk - Nq.  Work items are ordered heaviest first: rank r covers query
+// tile nqt-1-r of every unit when causal (tile r otherwise), each split of it
+// in turn.  An item may own no key tile (a split outside the tile's visible
+// range); every role skips such items.
 // kGeneral = false compiles the plain self-attention case only (Nq == Nk, no
 // window, one split, per-head tiles), so the common path carries none of the
 // general path's code.
 template <bool kGeneral>
 __device__ __forceinline__ Item decode_item(int idx, const FwdArgs& a) {
   const int splits = kGeneral ? a.splits : 1;
-  int rs, u;
-  if (a.causal) {
-    rs = idx / a.units;
-    u = idx - rs * a.units;
-  } else {
-    const int per = a.nqt * splits;
-    u = idx / per;
-    rs = idx - u * per;
-  }
+  const int rs = idx / a.units;
+  const int u = idx - rs * a.units;
   const int rank = rs / splits;
   Item it;
   it.split = rs - rank * splits;
@@ -438,20 +428,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;              // row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    // One slot per row is enough for the reference max: the owner of tile t+1
-    // reads it before it writes its own and only then arrives on the hand
-    // barrier the owner of tile t+2 waits for.
-    float* mref = reinterpret_cast<float*>(smem + L::kMref);   // [row]
-    float2* lxb = reinterpret_cast<float2*>(smem + L::kLx);    // [item parity][row]
+    float* mref = reinterpret_cast<float*>(smem + L::kMref);   // [tile parity][row]
+    float* lxb = reinterpret_cast<float*>(smem + L::kLx);      // [item parity][row]
     const float sl2 = args.scale_log2;
     const uint64_t sl2x2 = f2pack(sl2, sl2);
     float m_g = -INFINITY;                       // reference max this group's row sum is relative to
-    // This group's part of the row sum, twice: of the probabilities as
-    // computed (for LSE) and of their bf16 roundings, the weights the P V
-    // product actually applies (O is normalised by that sum, so each O row is
-    // exactly the convex combination of V rows the tensor core formed).
-    float l_g = 0.f, lr_g = 0.f;
-    int my_item = -1;                            // item the group's (l_g, lr_g, m_g) belong to
+    float l_g = 0.f;                             // this group's part of the row sum
+    int my_item = -1;                            // item the group's (l_g, m_g) belong to
     int n_multi = 0;                             // items with >= 2 tiles completed so far
     Cursor<kGeneral> c;
     c.init(args, n_items);
@@ -508,23 +491,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_prev = -INFINITY;
       if (t > 0) {
         if (!mbar_wait_warp(&bars->hand[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteHand)) break;
-        if (j > 0) m_prev = mref[r];
+        if (j > 0) m_prev = mref[((t - 1) & 1) * 128 + r];
       }
       const bool need = (j == 0) || (m_cand > m_prev + kRescaleThreshold);
       const float m_new = need ? m_cand : m_prev;
       // Hand the reference on to the owner of tile t+1 right away.
-      mref[r] = m_new;
+      mref[(t & 1) * 128 + r] = m_new;
       mbar_arrive(&bars->hand[t & 1]);
 
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       if (my_item != c.item) {
         my_item = c.item;
         l_g = 0.f;
-        lr_g = 0.f;
       } else if (m_g != m_new) {
-        const float a = ex2(m_g - m_use);
-        l_g *= a;
-        lr_g *= a;
+        l_g *= ex2(m_g - m_use);
       }
       m_g = m_new;
 
@@ -534,14 +514,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tP = tmem + 256 + buf * 64 + lane_off;
       const uint64_t negm = f2pack(-m_use, -m_use);
-      uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;   // sums of P~
-      uint64_t rac0 = 0, rac1 = 0;                      // sums of bf16(P~)
+      uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
-          uint64_t x[4], xr[4];
+          uint64_t x[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint64_t sv = f2pack(__uint_as_float(sr[q][e + 2 * u]), __uint_as_float(sr[q][e + 2 * u + 1]));
@@ -550,26 +529,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo = ex2(lo);
             hi = ex2(hi);
             x[u] = f2pack(lo, hi);
-            const uint32_t w = cvt_bf16x2(lo, hi);
-            pk[e / 2 + u] = w;
-            // The two bf16 halves as fp32: the low one shifted up, the high
-            // one with the low half cleared.
-            xr[u] = f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+            pk[e / 2 + u] = cvt_bf16x2(lo, hi);
           }
           acc0 = fadd2(acc0, x[0]);
           acc1 = fadd2(acc1, x[1]);
           acc2 = fadd2(acc2, x[2]);
           acc3 = fadd2(acc3, x[3]);
-          rac0 = fadd2(rac0, fadd2(xr[0], xr[1]));
-          rac1 = fadd2(rac1, fadd2(xr[2], xr[3]));
         }
         tmem_st16(tP + q * 16, pk);
       }
       float a0, a1;
       f2unpack(fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3)), a0, a1);
       l_g += a0 + a1;
-      f2unpack(fadd2(rac0, rac1), a0, a1);
-      lr_g += a0 + a1;
 
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // O holds rows relative to the previous reference: rescale it once
@@ -601,18 +572,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j == n - 2) {
         // The other group owns the item's last tile: hand it this group's
         // row-sum part, relative to m_new (which it reads back as m_prev).
-        lxb[multi_slot * 128 + r] = make_float2(l_g, lr_g);
+        lxb[multi_slot * 128 + r] = l_g;
         mbar_arrive(&bars->lx[multi_slot]);
       }
       if (j == n - 1) {
         // ------------------------------------------------ epilogue of the item
-        float l_tot = l_g, lr_tot = lr_g;
+        float l_tot = l_g;
         if (n >= 2) {
           if (!mbar_wait_warp(&bars->lx[multi_slot], (n_multi_before >> 1) & 1, st, abort_flag, kSiteLx)) break;
-          const float2 lo = lxb[multi_slot * 128 + r];
-          const float a = ex2(m_prev - m_use);
-          l_tot += lo.x * a;
-          lr_tot += lo.y * a;
+          l_tot += lxb[multi_slot * 128 + r] * ex2(m_prev - m_use);
         }
         if (!mbar_wait_warp(&bars->o_done[t & 1], (t >> 1) & 1, st, abort_flag, kSiteOLast)) break;
         tc_fence_after();
@@ -624,30 +592,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           // columns at a time; the Q / K producer then writes the tile with
           // TMA stores (rows past N are clipped) before it reloads the slot.
           // The group neither stores rows nor waits for the store.
-          // The whole O row goes to registers first, so the next item's first
-          // P V may overwrite O while this row is normalised and staged.
-          uint32_t o[D / 32][32];
-#pragma unroll
-          for (int q = 0; q < D / 32; ++q) tmem_ld32(tO + lane_off + q * 32, o[q]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < D / 32; ++q) reg_fence(o[q]);
-          tc_fence_before();
-          mbar_arrive(&bars->o_free);
-          const float inv_l = 1.f / lr_tot;
+          const float inv_l = 1.f / l_tot;
           const uint32_t stage = smem_u32(smem + L::kQ) + (c.li & 1) * L::kTile;
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
+          for (int a = 0; a < kAtoms; ++a) {
+            uint32_t o[2][32];
+            tmem_ld32(tO + lane_off + a * 64, o[0]);
+            tmem_ld32(tO + lane_off + a * 64 + 32, o[1]);
+            tmem_wait_ld();
+            reg_fence(o[0]);
+            reg_fence(o[1]);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint32_t w0 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 0]) * inv_l, __uint_as_float(o[q][v * 8 + 1]) * inv_l);
-              const uint32_t w1 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 2]) * inv_l, __uint_as_float(o[q][v * 8 + 3]) * inv_l);
-              const uint32_t w2 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 4]) * inv_l, __uint_as_float(o[q][v * 8 + 5]) * inv_l);
-              const uint32_t w3 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 6]) * inv_l, __uint_as_float(o[q][v * 8 + 7]) * inv_l);
-              // Columns q*32 + v*8 .. +7: block q / 2, 16-byte chunk (q % 2) * 4 + v.
-              st_shared_v4(stage + (q >> 1) * kBlockBytes + swz128(r, (q & 1) * 4 + v), w0, w1, w2, w3);
+            for (int q = 0; q < 2; ++q) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const uint32_t w0 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 0]) * inv_l, __uint_as_float(o[q][v * 8 + 1]) * inv_l);
+                const uint32_t w1 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 2]) * inv_l, __uint_as_float(o[q][v * 8 + 3]) * inv_l);
+                const uint32_t w2 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 4]) * inv_l, __uint_as_float(o[q][v * 8 + 5]) * inv_l);
+                const uint32_t w3 = cvt_bf16x2(__uint_as_float(o[q][v * 8 + 6]) * inv_l, __uint_as_float(o[q][v * 8 + 7]) * inv_l);
+                // Columns a*64 + q*32 + v*8 .. +7: block a, 16-byte chunk q*4 + v.
+                st_shared_v4(stage + a * kBlockBytes + swz128(r, q * 4 + v), w0, w1, w2, w3);
+              }
             }
           }
+          tc_fence_before();
+          mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
           if (r < c.it.rows) args.lse[frow] = (m_new + __log2f(l_tot)) * 0.69314718055994530942f;
           fence_proxy_async_smem();
           mbar_arrive(&bars->o_staged[c.li & 1]);   // the Q / K producer stores it
@@ -662,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
           if (r < c.it.rows) {
             if (args.splits == 1) {
-              const float inv_l = 1.f / lr_tot;
+              const float inv_l = 1.f / l_tot;
               __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.o) + frow * D;
 #pragma unroll
               for (int q = 0; q < D / 32; ++q) {
@@ -681,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // One key split: O normalised within the split, fp32, and its LSE;
               // a row that sees no key of the split gets O = 0, LSE = -inf.
               const long long prow = (long long)c.it.split * args.B * args.Hq * args.Nq + frow;
-              const float inv_l = lr_tot > 0.f ? 1.f / lr_tot : 0.f;
+              const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
               float4* orow = reinterpret_cast<float4*>(args.o_part + prow * D);
 #pragma unroll
               for (int q = 0; q < D / 32; ++q)
