@@ -72,9 +72,9 @@ struct FwdCfg {
   static constexpr uint32_t kQ = 0;                              // 2 slots
   static constexpr uint32_t kK = kQ + 2u * kTile;
   static constexpr uint32_t kV = kK + kStagesK * kTile;
-  static constexpr uint32_t kMref = kV + kStagesV * kTile;     // reference-max hand-off, 2 x 128 fp32
-  static constexpr uint32_t kLx = kMref + 1024u;               // row-sum hand-off, 2 x 128 fp32
-  static constexpr uint32_t kBar = kLx + 1024u;
+  static constexpr uint32_t kMref = kV + kStagesV * kTile;     // reference-max hand-off, 128 fp32
+  static constexpr uint32_t kLx = kMref + 512u;                // row-sum hand-off, 2 x 128 float2
+  static constexpr uint32_t kBar = kLx + 2048u;
   static constexpr uint32_t kBytes = kBar + 512u;
 };
 
@@ -428,13 +428,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;              // row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    float* mref = reinterpret_cast<float*>(smem + L::kMref);   // [tile parity][row]
-    float* lxb = reinterpret_cast<float*>(smem + L::kLx);      // [item parity][row]
+    // One slot per row is enough for the reference max: the owner of tile t+1
+    // reads it before it writes its own and only then arrives on the hand
+    // barrier the owner of tile t+2 waits for.
+    float* mref = reinterpret_cast<float*>(smem + L::kMref);   // [row]
+    float2* lxb = reinterpret_cast<float2*>(smem + L::kLx);    // [item parity][row]
     const float sl2 = args.scale_log2;
     const uint64_t sl2x2 = f2pack(sl2, sl2);
     float m_g = -INFINITY;                       // reference max this group's row sum is relative to
     float l_g = 0.f;                             // this group's part of the row sum
-    int my_item = -1;                            // item the group's (l_g, m_g) belong to
+    // The P V product applies each probability rounded to bf16.  A row's
+    // largest probability in a tile is 2^lag with a non-integer lag whenever
+    // the reference max lags the row's max, so its rounding (relative 2^-9)
+    // would not cancel against the row sum; c_g collects, per tile, that one
+    // weight's rounding, and O is normalised by l + c (LSE by l).  On rows
+    // dominated by one key this keeps O the convex combination the tensor
+    // core formed; the other weights' roundings average out.
+    float c_g = 0.f;
+    int my_item = -1;                            // item the group's (l_g, c_g, m_g) belong to
     int n_multi = 0;                             // items with >= 2 tiles completed so far
     Cursor<kGeneral> c;
     c.init(args, n_items);
@@ -483,7 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx3 = fmax3(mx3, __uint_as_float(sr[q][e + 6]), __uint_as_float(sr[q][e + 7]));
         }
       }
-      const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float s_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float m_cand = s_max * sl2;
       // Reference max after the previous tile (owned by the other group).  The
       // wait also happens at an item's first tile, where the value is unused:
       // it keeps the two groups' hand-offs strictly alternating, so no hand
@@ -491,22 +503,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_prev = -INFINITY;
       if (t > 0) {
         if (!mbar_wait_warp(&bars->hand[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteHand)) break;
-        if (j > 0) m_prev = mref[((t - 1) & 1) * 128 + r];
+        if (j > 0) m_prev = mref[r];
       }
       const bool need = (j == 0) || (m_cand > m_prev + kRescaleThreshold);
       const float m_new = need ? m_cand : m_prev;
       // Hand the reference on to the owner of tile t+1 right away.
-      mref[(t & 1) * 128 + r] = m_new;
+      mref[r] = m_new;
       mbar_arrive(&bars->hand[t & 1]);
 
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       if (my_item != c.item) {
         my_item = c.item;
         l_g = 0.f;
+        c_g = 0.f;
       } else if (m_g != m_new) {
-        l_g *= ex2(m_g - m_use);
+        const float a = ex2(m_g - m_use);
+        l_g *= a;
+        c_g *= a;
       }
       m_g = m_new;
+      {
+        // The tile's largest probability exactly as the loop below forms it,
+        // and its bf16 rounding error (0 for a row the tile masks entirely).
+        const float p_max = ex2(fmaf(s_max, sl2, -m_use));
+        c_g += __uint_as_float(cvt_bf16x2(p_max, 0.f) << 16) - p_max;
+      }
 
       // P = 2^(s*sl2 - m), 32 keys at a time, into probability buffer t % 2
       // once P V_{t-2} has consumed it.
@@ -571,17 +592,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (j == n - 2) {
         // The other group owns the item's last tile: hand it this group's
-        // row-sum part, relative to m_new (which it reads back as m_prev).
-        lxb[multi_slot * 128 + r] = l_g;
+        // row-sum part and rounding correction, relative to m_new (which it
+        // reads back as m_prev).
+        lxb[multi_slot * 128 + r] = make_float2(l_g, c_g);
         mbar_arrive(&bars->lx[multi_slot]);
       }
       if (j == n - 1) {
         // ------------------------------------------------ epilogue of the item
-        float l_tot = l_g;
+        float l_tot = l_g, c_tot = c_g;
         if (n >= 2) {
           if (!mbar_wait_warp(&bars->lx[multi_slot], (n_multi_before >> 1) & 1, st, abort_flag, kSiteLx)) break;
-          l_tot += lxb[multi_slot * 128 + r] * ex2(m_prev - m_use);
+          const float2 other = lxb[multi_slot * 128 + r];
+          const float a = ex2(m_prev - m_use);
+          l_tot += other.x * a;
+          c_tot += other.y * a;
         }
+        const float l_o = l_tot + c_tot;   // sum of the weights P V applied
         if (!mbar_wait_warp(&bars->o_done[t & 1], (t >> 1) & 1, st, abort_flag, kSiteOLast)) break;
         tc_fence_after();
         const long long frow = c.it.row0 + r;
@@ -592,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // columns at a time; the Q / K producer then writes the tile with
           // TMA stores (rows past N are clipped) before it reloads the slot.
           // The group neither stores rows nor waits for the store.
-          const float inv_l = 1.f / l_tot;
+          const float inv_l = 1.f / l_o;
           const uint32_t stage = smem_u32(smem + L::kQ) + (c.li & 1) * L::kTile;
 #pragma unroll
           for (int a = 0; a < kAtoms; ++a) {
@@ -631,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
           if (r < c.it.rows) {
             if (args.splits == 1) {
-              const float inv_l = 1.f / l_tot;
+              const float inv_l = 1.f / l_o;
               __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.o) + frow * D;
 #pragma unroll
               for (int q = 0; q < D / 32; ++q) {
@@ -650,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // One key split: O normalised within the split, fp32, and its LSE;
               // a row that sees no key of the split gets O = 0, LSE = -inf.
               const long long prow = (long long)c.it.split * args.B * args.Hq * args.Nq + frow;
-              const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+              const float inv_l = l_tot > 0.f ? 1.f / l_o : 0.f;
               float4* orow = reinterpret_cast<float4*>(args.o_part + prow * D);
 #pragma unroll
               for (int q = 0; q < D / 32; ++q)

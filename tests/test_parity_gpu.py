@@ -53,7 +53,9 @@ def test_workload_full_parity(cuda_lib, name):
 SAMPLED = {
     "gqa_causal_b2_hq32_hkv8_n8192_d128": 2,
     "long_causal_b1_h16_n32768_d128": 1,
-    "stressed_b8_h32_n4096_d64": 4,
+    # Peaked rows (q, k ~ N(0, 9)): where the rounding of a dominant weight
+    # shows, so more of its heads are checked.
+    "stressed_b8_h32_n4096_d64": 16,
 }
 
 
