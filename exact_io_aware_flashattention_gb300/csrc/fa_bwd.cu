@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kAtoms = D / 64;
   constexpr int kHalfD = D / 2;
   constexpr int kPasses = kHalfD / 32;   // 32-column dQ staging passes per group
+  constexpr bool kWarpIssue = true;        // see the MMA issuer
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBar);
   volatile int* abort_flag = &bars->abort;
@@ -293,7 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // kWarpIssue: the whole warp runs the issuer loop, every lane polls the
+    // barriers and elect.sync picks the lane that issues each MMA and commit
+    // (a converged warp issues tcgen05.mma faster than a lone lane); else
+    // lane 0 alone.
+    auto wait = [&](uint64_t* bar, uint32_t parity, int site) {
+      return issuer_wait<kWarpIssue>(bar, parity, st, abort_flag, site);
+    };
+    auto ss = [](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) { issue_ss<kWarpIssue>(d, a, b, id, acc); };
+    auto ts = [](uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) { issue_ts<kWarpIssue>(d, a, b, id, acc); };
+    auto commit = [](uint64_t* bar) { issue_commit<kWarpIssue>(bar); };
+    if (kWarpIssue || lane == 0) {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);   // S^T, dP^T
       constexpr uint32_t idKM = idesc_bf16(128, D, false, true);      // dV, dK
       constexpr uint32_t idMM = idesc_bf16(128, D, true, true);       // dQ
@@ -310,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int uidx = unit_of_round(round);
         if (uidx >= n_units) break;
         const Unit un = decode_unit<kHeadMajor>(uidx, args, nt);
-        if (!mbar_wait(&bars->kv_full, nu & 1, st, abort_flag, kSiteKV)) break;
+        if (!wait(&bars->kv_full, nu & 1, kSiteKV)) break;
       for (int t = 0; ok && t < un.n_items; ++t) {
         const int tg = T + t;
         const int slot = tg & 1;
@@ -319,30 +330,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t pph = (tg - 1) & 1;   // previous item's phase
         const uint64_t dQk = slot ? dQk1 : dQk0, dOk = slot ? dOk1 : dOk0;
         const uint64_t dQm = slot ? dQm1 : dQm0, dOm = slot ? dOm1 : dOm0;
-        if (!mbar_wait(&bars->q_full[slot], sph, st, abort_flag, kSiteQFull)) { ok = false; break; }
+        if (!wait(&bars->q_full[slot], sph, kSiteQFull)) { ok = false; break; }
         // S_{t+1} overwrites the score region, which holds P^T_t (read by dV_t)
         // and dS^T_t (read by dK_t); dK_t is the later of the two.
-        if (tg > 0 && !mbar_wait(&bars->dk_done, pph, st, abort_flag, kSiteDkDone)) { ok = false; break; }
+        if (tg > 0 && !wait(&bars->dk_done, pph, kSiteDkDone)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
-          mma_bf16_ss(tS, dKk + desc_step_kmajor(k16, kBlockBytes), dQk + desc_step_kmajor(k16, kBlockBytes), idSS,
+          ss(tS, dKk + desc_step_kmajor(k16, kBlockBytes), dQk + desc_step_kmajor(k16, kBlockBytes), idSS,
                       k16 > 0);
-        mma_commit(&bars->s_full);
-        if (!mbar_wait(&bars->do_full[slot], sph, st, abort_flag, kSiteDoFull)) { ok = false; break; }
+        commit(&bars->s_full);
+        if (!wait(&bars->do_full[slot], sph, kSiteDoFull)) { ok = false; break; }
         // dP_t overwrites the dQ partial of item t-1 (read out by then) or,
         // without dQ, dP^T of item t-1 (read before ds_full of t-1).
-        if (kDq && tg > 0 && !mbar_wait(&bars->dq_empty, pph, st, abort_flag, kSiteDqEmpty)) { ok = false; break; }
+        if (kDq && tg > 0 && !wait(&bars->dq_empty, pph, kSiteDqEmpty)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k16 = 0; k16 < D / 16; ++k16)
-          mma_bf16_ss(tDP, dVk + desc_step_kmajor(k16, kBlockBytes), dOk + desc_step_kmajor(k16, kBlockBytes), idSS,
+          ss(tDP, dVk + desc_step_kmajor(k16, kBlockBytes), dOk + desc_step_kmajor(k16, kBlockBytes), idSS,
                       k16 > 0);
-        mma_commit(&bars->dp_full);
-        if (!mbar_wait(&bars->p_full, ph, st, abort_flag, kSitePFull)) { ok = false; break; }
+        commit(&bars->dp_full);
+        if (!wait(&bars->p_full, ph, kSitePFull)) { ok = false; break; }
         // The unit's first dV / dK overwrite the previous unit's accumulators:
         // its epilogue must have read them out.
-        if (t == 0 && nu > 0 && !mbar_wait(&bars->dkv_free, (nu - 1) & 1, st, abort_flag, kSiteDkvDone)) {
+        if (t == 0 && nu > 0 && !wait(&bars->dkv_free, (nu - 1) & 1, kSiteDkvDone)) {
           ok = false;
           break;
         }
@@ -350,32 +361,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P^T for query columns 16*k16.. lives at column (k16/4)*64 + (k16%4)*8.
 #pragma unroll
         for (int k16 = 0; k16 < kT / 16; ++k16)
-          mma_bf16_ts(tDV, tS + (k16 >> 2) * 64 + (k16 & 3) * 8, dOm + desc_step_mnmajor(k16), idKM,
+          ts(tDV, tS + (k16 >> 2) * 64 + (k16 & 3) * 8, dOm + desc_step_mnmajor(k16), idKM,
                       (t > 0 || k16 > 0) ? 1u : 0u);
-        mma_commit(&bars->do_empty[slot]);
-        if (!mbar_wait(&bars->ds_full, ph, st, abort_flag, kSiteDsFull)) { ok = false; break; }
+        commit(&bars->do_empty[slot]);
+        if (!wait(&bars->ds_full, ph, kSiteDsFull)) { ok = false; break; }
         tc_fence_after();
         // dS^T for query columns 16*k16.. lives at column (k16/4)*64 + 32 + (k16%4)*8.
 #pragma unroll
         for (int k16 = 0; k16 < kT / 16; ++k16)
-          mma_bf16_ts(tDK, tS + (k16 >> 2) * 64 + 32 + (k16 & 3) * 8, dQm + desc_step_mnmajor(k16), idKM,
+          ts(tDK, tS + (k16 >> 2) * 64 + 32 + (k16 & 3) * 8, dQm + desc_step_mnmajor(k16), idKM,
                       (t > 0 || k16 > 0) ? 1u : 0u);
-        mma_commit(&bars->dk_done);
+        commit(&bars->dk_done);
         if (kDq) {
 #pragma unroll
           for (int k16 = 0; k16 < kT / 16; ++k16)
-            mma_bf16_ss(tDP, dDSm + desc_step_mnmajor(k16), dKm + desc_step_mnmajor(k16), idMM,
+            ss(tDP, dDSm + desc_step_mnmajor(k16), dKm + desc_step_mnmajor(k16), idMM,
                         k16 > 0 ? 1u : 0u);
-          mma_commit(&bars->dq_full);
+          commit(&bars->dq_full);
         }
-        mma_commit(&bars->q_empty[slot]);
+        commit(&bars->q_empty[slot]);
       }
       if (!ok) break;
-      mma_commit(&bars->dkv_done);
-      mma_commit(&bars->kv_empty);
+      commit(&bars->dkv_done);
+      commit(&bars->kv_empty);
       T += un.n_items;
       }
-      mma_commit(&bars->drain);
+      commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, st, kDrainMma);
     }
   } else if (warp < 10) {

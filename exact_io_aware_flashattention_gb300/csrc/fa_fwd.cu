@@ -214,6 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = FwdCfg<D>;
   constexpr int kAtoms = D / 64;
   constexpr int SK = L::kStagesK, SV = L::kStagesV;
+  // The MMA issuers run as one lane each (a whole-warp issuer, see
+  // issuer_wait, spills in the 56-register control warpgroup).
+  constexpr bool kWarpIssue = false;
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBar);
   volatile int* abort_flag = &bars->abort;
@@ -364,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 1) {
       // ------------------------------------------------------ S issuer
-      if (lane == 0) {
+      if (kWarpIssue || lane == 0) {
         constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
         // Operand descriptors, built once: a K stage or a k16 step adds a constant.
         const uint64_t dQ0 = desc_kmajor(sQ, 0, kBlockBytes), dQ1 = desc_kmajor(sQ + L::kTile, 0, kBlockBytes);
@@ -374,50 +377,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ts = 0; sc.valid; ++ts, sc.next(args)) {
           const int buf = ts % kSBuf;
           // S_ts reuses score buffer ts % 2 once the owner of tile ts-2 has read it.
-          if (ts >= 2 && !mbar_wait(&bars->s_free[buf], ((ts - 2) / kSBuf) & 1, st, abort_flag, kSiteSFree)) break;
+          if (ts >= 2 && !issuer_wait<kWarpIssue>(&bars->s_free[buf], ((ts - 2) / kSBuf) & 1, st, abort_flag, kSiteSFree)) break;
           if (sc.j == 0 &&
-              !mbar_wait(&bars->q_full[sc.li & 1], (sc.li >> 1) & 1, st, abort_flag, kSiteQFull))
+              !issuer_wait<kWarpIssue>(&bars->q_full[sc.li & 1], (sc.li >> 1) & 1, st, abort_flag, kSiteQFull))
             break;
           const int s = ts % SK;
-          if (!mbar_wait(&bars->k_full[s], (ts / SK) & 1, st, abort_flag, kSiteKFull)) break;
+          if (!issuer_wait<kWarpIssue>(&bars->k_full[s], (ts / SK) & 1, st, abort_flag, kSiteKFull)) break;
           tc_fence_after();
           const uint64_t dq = (sc.li & 1) ? dQ1 : dQ0;
           const uint64_t dk = dK0 + (uint64_t)s * (L::kTile >> 4);
 #pragma unroll
           for (int k16 = 0; k16 < D / 16; ++k16)
-            mma_bf16_ss(tmem + buf * 128, dq + desc_step_kmajor(k16, kBlockBytes), dk + desc_step_kmajor(k16, kBlockBytes),
+            issue_ss<kWarpIssue>(tmem + buf * 128, dq + desc_step_kmajor(k16, kBlockBytes), dk + desc_step_kmajor(k16, kBlockBytes),
                         idS, k16 > 0);
-          mma_commit(&bars->s_full[buf]);
-          mma_commit(&bars->k_empty[s]);
-          if (sc.j == sc.it.n - 1) mma_commit(&bars->q_empty[sc.li & 1]);
+          issue_commit<kWarpIssue>(&bars->s_full[buf]);
+          issue_commit<kWarpIssue>(&bars->k_empty[s]);
+          if (sc.j == sc.it.n - 1) issue_commit<kWarpIssue>(&bars->q_empty[sc.li & 1]);
         }
         // No MMA may still be writing tensor memory when it is freed.
-        mma_commit(&bars->drain_s);
+        issue_commit<kWarpIssue>(&bars->drain_s);
         mbar_wait_drain(&bars->drain_s, 0, st, kDrainS);
       }
     } else if (warp == 3) {
       // ------------------------------------------------------ P V issuer
-      if (lane == 0) {
+      if (kWarpIssue || lane == 0) {
         constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
         const uint64_t dV0 = desc_mnmajor(sV, 0, kBlockBytes);
         Cursor<kGeneral> pc;
         pc.init(args, n_items);
         for (int t = 0; pc.valid; ++t, pc.next(args)) {
           const int buf = t % kSBuf;
-          if (!mbar_wait(&bars->p_full[buf], (t / kSBuf) & 1, st, abort_flag, kSitePFull)) break;
+          if (!issuer_wait<kWarpIssue>(&bars->p_full[buf], (t / kSBuf) & 1, st, abort_flag, kSitePFull)) break;
           const int v = t % SV;
-          if (!mbar_wait(&bars->v_full[v], (t / SV) & 1, st, abort_flag, kSiteVFull)) break;
-          if (pc.j == 0 && pc.li > 0 && !mbar_wait(&bars->o_free, (pc.li - 1) & 1, st, abort_flag, kSiteOFree)) break;
+          if (!issuer_wait<kWarpIssue>(&bars->v_full[v], (t / SV) & 1, st, abort_flag, kSiteVFull)) break;
+          if (pc.j == 0 && pc.li > 0 && !issuer_wait<kWarpIssue>(&bars->o_free, (pc.li - 1) & 1, st, abort_flag, kSiteOFree)) break;
           tc_fence_after();
           const uint64_t dv = dV0 + (uint64_t)v * (L::kTile >> 4);
 #pragma unroll
           for (int k16 = 0; k16 < kBN / 16; ++k16)
-            mma_bf16_ts(tO, tmem + 256 + buf * 64 + k16 * 8, dv + desc_step_mnmajor(k16), idO,
+            issue_ts<kWarpIssue>(tO, tmem + 256 + buf * 64 + k16 * 8, dv + desc_step_mnmajor(k16), idO,
                         (pc.j > 0 || k16 > 0) ? 1u : 0u);
-          mma_commit(&bars->o_done[t & 1]);
-          mma_commit(&bars->v_empty[v]);
+          issue_commit<kWarpIssue>(&bars->o_done[t & 1]);
+          issue_commit<kWarpIssue>(&bars->v_empty[v]);
         }
-        mma_commit(&bars->drain_pv);
+        issue_commit<kWarpIssue>(&bars->drain_pv);
         mbar_wait_drain(&bars->drain_pv, 0, st, kDrainPV);
       }
     }

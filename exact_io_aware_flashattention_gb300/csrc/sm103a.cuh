@@ -276,12 +276,68 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// The same two MMAs for a converged warp: every lane executes the call and
+// elect.sync picks one lane (the lowest, lane 0 of a full warp) to issue.
+__device__ __forceinline__ void mma_bf16_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive (once) on *bar when every tcgen05 async operation issued so far by
 // this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// mma_commit from the lane elect.sync picks in a converged warp (the lane
+// that issued the warp's MMAs).
+__device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+// An MMA-issuing role run by one lane (kWarp = false) or by a whole converged
+// warp (kWarp = true: every lane polls the barriers, the warp agrees on the
+// outcome, and elect.sync picks the lane that issues each MMA and commit).
+template <bool kWarp>
+__device__ __forceinline__ bool issuer_wait(uint64_t* bar, uint32_t parity, const DevStatus& st, volatile int* abort,
+                                            int site) {
+  bool r = mbar_wait(bar, parity, st, abort, site);
+  if constexpr (kWarp) r = __all_sync(0xffffffffu, r);
+  return r;
+}
+template <bool kWarp>
+__device__ __forceinline__ void issue_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (kWarp) mma_bf16_ss_warp(d, a, b, idesc, acc); else mma_bf16_ss(d, a, b, idesc, acc);
+}
+template <bool kWarp>
+__device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (kWarp) mma_bf16_ts_warp(d, a, b, idesc, acc); else mma_bf16_ts(d, a, b, idesc, acc);
+}
+template <bool kWarp>
+__device__ __forceinline__ void issue_commit(uint64_t* bar) {
+  if constexpr (kWarp) mma_commit_warp(bar); else mma_commit(bar);
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives lane
