@@ -73,8 +73,11 @@ struct FwdCfg {
   static constexpr uint32_t kK = kQ + 2u * kTile;
   static constexpr uint32_t kV = kK + kStagesK * kTile;
   static constexpr uint32_t kMref = kV + kStagesV * kTile;     // reference-max hand-off, 128 fp32
-  static constexpr uint32_t kLx = kMref + 512u;                // row-sum hand-off, 2 x 128 float2
-  static constexpr uint32_t kBar = kLx + 2048u;
+  // Row-sum hand-off, 2 x 128 entries: float2 (sum, correction), or, with
+  // one O accumulator per softmax group (d = 64), float4 (sum, correction,
+  // reference max, unused).
+  static constexpr uint32_t kLx = kMref + 512u;
+  static constexpr uint32_t kBar = kLx + (D == 64 ? 4096u : 2048u);
   static constexpr uint32_t kBytes = kBar + 512u;
 };
 
@@ -217,6 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The MMA issuers run as one lane each (a whole-warp issuer, see
   // issuer_wait, spills in the 56-register control warpgroup).
   constexpr bool kWarpIssue = false;
+  // d = 64: each softmax group accumulates its own tiles into its own O
+  // (64 columns each, at 384 and 448) relative to its own reference max, so
+  // a tile never waits for the other group's max; the item's epilogue
+  // combines the two (O = O_0 2^(m_0 - m) + O_1 2^(m_1 - m), likewise the
+  // row sums, m = max(m_0, m_1)).  d = 128 has no tensor memory for a second
+  // O: one shared O and the reference max handed from tile to tile.
+  constexpr bool kIndep = D == 64;
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBar);
   volatile int* abort_flag = &bars->abort;
@@ -415,8 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t dv = dV0 + (uint64_t)v * (L::kTile >> 4);
 #pragma unroll
           for (int k16 = 0; k16 < kBN / 16; ++k16)
-            issue_ts<kWarpIssue>(tO, tmem + 256 + buf * 64 + k16 * 8, dv + desc_step_mnmajor(k16), idO,
-                        (pc.j > 0 || k16 > 0) ? 1u : 0u);
+            issue_ts<kWarpIssue>(tO + (kIndep ? (uint32_t)(t & 1) * 64u : 0u), tmem + 256 + buf * 64 + k16 * 8,
+                                 dv + desc_step_mnmajor(k16), idO,
+                                 (pc.j >= (kIndep ? 2 : 1) || k16 > 0) ? 1u : 0u);
           issue_commit<kWarpIssue>(&bars->o_done[t & 1]);
           issue_commit<kWarpIssue>(&bars->v_empty[v]);
         }
@@ -438,6 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float2* lxb = reinterpret_cast<float2*>(smem + L::kLx);    // [item parity][row]
     const float sl2 = args.scale_log2;
     const uint64_t sl2x2 = f2pack(sl2, sl2);
+    const uint32_t tOg = kIndep ? tO + (uint32_t)g * 64u : tO;          // this group's O
+    const uint32_t tOo = kIndep ? tO + (uint32_t)(1 - g) * 64u : tO;    // the other group's
     float m_g = -INFINITY;                       // reference max this group's row sum is relative to
     float l_g = 0.f;                             // this group's part of the row sum
     // The P V product applies each probability rounded to bf16.  A row's
@@ -504,15 +517,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // it keeps the two groups' hand-offs strictly alternating, so no hand
       // barrier can run two phases ahead of its waiter.
       float m_prev = -INFINITY;
-      if (t > 0) {
-        if (!mbar_wait_warp(&bars->hand[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteHand)) break;
-        if (j > 0) m_prev = mref[r];
+      bool first_g;                              // the group's first tile of the item
+      if constexpr (kIndep) {
+        first_g = my_item != c.item;
+        if (!first_g) m_prev = m_g;
+      } else {
+        first_g = j == 0;
+        if (t > 0) {
+          if (!mbar_wait_warp(&bars->hand[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteHand)) break;
+          if (j > 0) m_prev = mref[r];
+        }
       }
-      const bool need = (j == 0) || (m_cand > m_prev + kRescaleThreshold);
+      const bool need = first_g || (m_cand > m_prev + kRescaleThreshold);
       const float m_new = need ? m_cand : m_prev;
-      // Hand the reference on to the owner of tile t+1 right away.
-      mref[r] = m_new;
-      mbar_arrive(&bars->hand[t & 1]);
+      if constexpr (!kIndep) {
+        // Hand the reference on to the owner of tile t+1 right away.
+        mref[r] = m_new;
+        mbar_arrive(&bars->hand[t & 1]);
+      }
 
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       if (my_item != c.item) {
@@ -566,17 +588,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       f2unpack(fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3)), a0, a1);
       l_g += a0 + a1;
 
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
+      if (!first_g && __any_sync(0xffffffffu, need)) {
         // O holds rows relative to the previous reference: rescale it once
-        // P V of the previous tile has landed.
+        // P V of the previous tile has landed (with one O per group, that is
+        // the group's own previous tile, already waited for above).
         const float alpha = need ? ex2(m_prev - m_use) : 1.f;
-        if (!mbar_wait_warp(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteORescale)) break;
+        if constexpr (!kIndep) {
+          if (!mbar_wait_warp(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, st, abort_flag, kSiteORescale)) break;
+        }
         tc_fence_after();
         const uint64_t al2 = f2pack(alpha, alpha);
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
           uint32_t o[32];
-          tmem_ld32(tO + lane_off + q * 32, o);
+          tmem_ld32(tOg + lane_off + q * 32, o);
           tmem_wait_ld();
           reg_fence(o);
 #pragma unroll
@@ -586,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             o[e] = __float_as_uint(lo);
             o[e + 1] = __float_as_uint(hi);
           }
-          tmem_st32(tO + lane_off + q * 32, o);
+          tmem_st32(tOg + lane_off + q * 32, o);
         }
       }
       tmem_wait_st();
@@ -597,20 +622,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The other group owns the item's last tile: hand it this group's
         // row-sum part and rounding correction, relative to m_new (which it
         // reads back as m_prev).
-        lxb[multi_slot * 128 + r] = make_float2(l_g, c_g);
+        if constexpr (kIndep)
+          reinterpret_cast<float4*>(lxb)[multi_slot * 128 + r] = make_float4(l_g, c_g, m_g, 0.f);
+        else
+          lxb[multi_slot * 128 + r] = make_float2(l_g, c_g);
         mbar_arrive(&bars->lx[multi_slot]);
       }
       if (j == n - 1) {
         // ------------------------------------------------ epilogue of the item
         float l_tot = l_g, c_tot = c_g;
+        float m_fin = m_new;                   // the reference the totals and O end up relative to
+        float a_g = 1.f, a_o = 0.f;            // weights of this group's and the other group's O
         if (n >= 2) {
           if (!mbar_wait_warp(&bars->lx[multi_slot], (n_multi_before >> 1) & 1, st, abort_flag, kSiteLx)) break;
-          const float2 other = lxb[multi_slot * 128 + r];
-          const float a = ex2(m_prev - m_use);
-          l_tot += other.x * a;
-          c_tot += other.y * a;
+          if constexpr (kIndep) {
+            const float4 other = reinterpret_cast<const float4*>(lxb)[multi_slot * 128 + r];
+            m_fin = fmaxf(m_new, other.z);
+            const float mf = m_fin == -INFINITY ? 0.f : m_fin;
+            a_g = ex2(m_new - mf);
+            a_o = ex2(other.z - mf);
+            l_tot = l_g * a_g + other.x * a_o;
+            c_tot = c_g * a_g + other.y * a_o;
+          } else {
+            const float2 other = lxb[multi_slot * 128 + r];
+            const float a = ex2(m_prev - m_use);
+            l_tot += other.x * a;
+            c_tot += other.y * a;
+          }
         }
         const float l_o = l_tot + c_tot;   // sum of the weights P V applied
+        // O row of this thread, in the same reference: one accumulator, or
+        // this group's and (items of two or more tiles) the other group's.
+        auto load_o = [&](int col, uint32_t (&dst)[32]) {
+          tmem_ld32(tOg + lane_off + col, dst);
+          if constexpr (kIndep) {
+            if (n >= 2) {
+              uint32_t oo[32];
+              tmem_ld32(tOo + lane_off + col, oo);
+              tmem_wait_ld();
+              reg_fence(dst);
+              reg_fence(oo);
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                dst[e] = __float_as_uint(__uint_as_float(dst[e]) * a_g + __uint_as_float(oo[e]) * a_o);
+            }
+          }
+        };
         if (!mbar_wait_warp(&bars->o_done[t & 1], (t >> 1) & 1, st, abort_flag, kSiteOLast)) break;
         tc_fence_after();
         const long long frow = c.it.row0 + r;
@@ -626,8 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int a = 0; a < kAtoms; ++a) {
             uint32_t o[2][32];
-            tmem_ld32(tO + lane_off + a * 64, o[0]);
-            tmem_ld32(tO + lane_off + a * 64 + 32, o[1]);
+            load_o(a * 64, o[0]);
+            load_o(a * 64 + 32, o[1]);
             tmem_wait_ld();
             reg_fence(o[0]);
             reg_fence(o[1]);
@@ -646,13 +703,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before();
           mbar_arrive(&bars->o_free);   // the next item's first P V may overwrite O now
-          if (r < c.it.rows) args.lse[frow] = (m_new + __log2f(l_tot)) * 0.69314718055994530942f;
+          if (r < c.it.rows) args.lse[frow] = (m_fin + __log2f(l_tot)) * 0.69314718055994530942f;
           fence_proxy_async_smem();
           mbar_arrive(&bars->o_staged[c.li & 1]);   // the Q / K producer stores it
         } else {
           uint32_t o[D / 32][32];
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) tmem_ld32(tO + lane_off + q * 32, o[q]);
+          for (int q = 0; q < D / 32; ++q) load_o(q * 32, o[q]);
           tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) reg_fence(o[q]);
@@ -674,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   *reinterpret_cast<uint4*>(orow + q * 32 + v * 8) = w;
                 }
               }
-              args.lse[frow] = (m_new + __log2f(l_tot)) * 0.69314718055994530942f;
+              args.lse[frow] = (m_fin + __log2f(l_tot)) * 0.69314718055994530942f;
             } else {
               // One key split: O normalised within the split, fp32, and its LSE;
               // a row that sees no key of the split gets O = 0, LSE = -inf.
@@ -690,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 __uint_as_float(o[q][v * 4 + 2]) * inv_l,
                                                 __uint_as_float(o[q][v * 4 + 3]) * inv_l);
               args.lse_part[prow] =
-                  l_tot > 0.f ? (m_new + __log2f(l_tot)) * 0.69314718055994530942f : -INFINITY;
+                  l_tot > 0.f ? (m_fin + __log2f(l_tot)) * 0.69314718055994530942f : -INFINITY;
             }
           }
         }
