@@ -222,7 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop (see issuer_wait in sm103a.cuh):
+    // every lane polls the barriers and elect.sync picks the issuing lane.
+    constexpr bool kWarpIssue = true;
+    {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);   // S, dP
       constexpr uint32_t idQ = idesc_bf16(128, D, false, true);       // dQ += dS K (K as the MN-major operand)
       // Operand descriptors, built once: a K / V stage or a k16 step adds a constant.
@@ -235,16 +238,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // waits until the previous item's dQ has been read out.
       auto issue_dq = [&](int tg, int jj, int ci) -> bool {
         const int x = tg & 1, s = tg % SK;
-        if (jj == 0 && ci > 0 && !mbar_wait(&bars->dq_free, (ci - 1) & 1, st, abort_flag, kSiteDqFree)) return false;
-        if (!mbar_wait(&bars->ds_full[x], (tg >> 1) & 1, st, abort_flag, kSiteDsFull)) return false;
+        if (jj == 0 && ci > 0 && !issuer_wait<kWarpIssue>(&bars->dq_free, (ci - 1) & 1, st, abort_flag, kSiteDqFree)) return false;
+        if (!issuer_wait<kWarpIssue>(&bars->ds_full[x], (tg >> 1) & 1, st, abort_flag, kSiteDsFull)) return false;
         tc_fence_after();
         const uint64_t dk = dKm + (uint64_t)s * (L::kTile >> 4);
 #pragma unroll
         for (int k16 = 0; k16 < kT / 16; ++k16)
-          mma_bf16_ts(tDQ, tmem + x * 128 + (k16 >> 2) * 64 + (k16 & 3) * 8, dk + desc_step_mnmajor(k16), idQ,
+          issue_ts<kWarpIssue>(tDQ, tmem + x * 128 + (k16 >> 2) * 64 + (k16 & 3) * 8, dk + desc_step_mnmajor(k16), idQ,
                       (jj > 0 || k16 > 0) ? 1u : 0u);
-        mma_commit(&bars->dq_done[x]);
-        mma_commit(&bars->k_empty[s]);
+        issue_commit<kWarpIssue>(&bars->dq_done[x]);
+        issue_commit<kWarpIssue>(&bars->k_empty[s]);
         return true;
       };
       bool ok = true;
@@ -253,40 +256,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u = item_of_round(k);
         if (u >= n_items) break;
         const int n = decode_item(u, args, nt).n;
-        if (!mbar_wait(&bars->q_full, ci & 1, st, abort_flag, kSiteQ)) break;
+        if (!issuer_wait<kWarpIssue>(&bars->q_full, ci & 1, st, abort_flag, kSiteQ)) break;
         for (int jj = 0; jj < n; ++jj) {
           const int tg = tiles + jj;
           const int x = tg & 1, s = tg % SK;
           // S_tg overwrites dS_{tg-2} (read by dQ_{tg-2}).
-          if (tg >= 2 && !mbar_wait(&bars->dq_done[x], ((tg - 2) >> 1) & 1, st, abort_flag, kSiteDqDone)) { ok = false; break; }
-          if (!mbar_wait(&bars->k_full[s], (tg / SK) & 1, st, abort_flag, kSiteKFull)) { ok = false; break; }
+          if (tg >= 2 && !issuer_wait<kWarpIssue>(&bars->dq_done[x], ((tg - 2) >> 1) & 1, st, abort_flag, kSiteDqDone)) { ok = false; break; }
+          if (!issuer_wait<kWarpIssue>(&bars->k_full[s], (tg / SK) & 1, st, abort_flag, kSiteKFull)) { ok = false; break; }
           tc_fence_after();
           const uint64_t dk = dKk + (uint64_t)s * (L::kTile >> 4);
 #pragma unroll
           for (int k16 = 0; k16 < D / 16; ++k16)
-            mma_bf16_ss(tmem + x * 128, dQk + desc_step_kmajor(k16, kBlockBytes),
+            issue_ss<kWarpIssue>(tmem + x * 128, dQk + desc_step_kmajor(k16, kBlockBytes),
                         dk + desc_step_kmajor(k16, kBlockBytes), idSS, k16 > 0);
-          mma_commit(&bars->s_full[x]);
+          issue_commit<kWarpIssue>(&bars->s_full[x]);
           // dP_tg overwrites dP_{tg-1}: the compute threads must have read it.
-          if (tg >= 1 && !mbar_wait(&bars->dp_free, (tg - 1) & 1, st, abort_flag, kSiteDpFree)) { ok = false; break; }
-          if (!mbar_wait(&bars->v_full[s], (tg / SK) & 1, st, abort_flag, kSiteVFull)) { ok = false; break; }
+          if (tg >= 1 && !issuer_wait<kWarpIssue>(&bars->dp_free, (tg - 1) & 1, st, abort_flag, kSiteDpFree)) { ok = false; break; }
+          if (!issuer_wait<kWarpIssue>(&bars->v_full[s], (tg / SK) & 1, st, abort_flag, kSiteVFull)) { ok = false; break; }
           tc_fence_after();
           const uint64_t dv = dVk + (uint64_t)s * (L::kTile >> 4);
 #pragma unroll
           for (int k16 = 0; k16 < D / 16; ++k16)
-            mma_bf16_ss(tDP, dOk + desc_step_kmajor(k16, kBlockBytes), dv + desc_step_kmajor(k16, kBlockBytes),
+            issue_ss<kWarpIssue>(tDP, dOk + desc_step_kmajor(k16, kBlockBytes), dv + desc_step_kmajor(k16, kBlockBytes),
                         idSS, k16 > 0);
-          mma_commit(&bars->dp_full);
-          mma_commit(&bars->v_empty[s]);
-          if (jj == n - 1) mma_commit(&bars->q_empty);   // the item's Q / dO are no longer read
+          issue_commit<kWarpIssue>(&bars->dp_full);
+          issue_commit<kWarpIssue>(&bars->v_empty[s]);
+          if (jj == n - 1) issue_commit<kWarpIssue>(&bars->q_empty);   // the item's Q / dO are no longer read
           if (jj >= 1 && !issue_dq(tg - 1, jj - 1, ci)) { ok = false; break; }
           if (jj == n - 1 && !issue_dq(tg, jj, ci)) { ok = false; break; }
         }
         if (!ok) break;
-        mma_commit(&bars->dq_final);
+        issue_commit<kWarpIssue>(&bars->dq_final);
         tiles += n;
       }
-      mma_commit(&bars->drain);
+      issue_commit<kWarpIssue>(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, st, kDrainMma);
     }
   } else {
