@@ -326,6 +326,15 @@ class Problem:
         self.ws_bytes = fa.fa_bwd_workspace_bytes(B, Hq, Hkv, N, d)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
 
+    def device_mib(self):
+        """Device memory the step needs: inputs, outputs and the backward's
+        workspace (the library allocates nothing itself), MiB; and the same as
+        a multiple of the O(N d) inputs."""
+        ts = (self.q, self.k, self.v, self.do, self.o, self.lse, self.dq, self.dk, self.dv, self.ws)
+        total = sum(t.numel() * t.element_size() for t in ts)
+        inputs = sum(t.numel() * t.element_size() for t in (self.q, self.k, self.v, self.do))
+        return {"step_buffers_mib": round(total / 2**20, 1), "x_inputs": round(total / inputs, 2)}
+
     def _call(self, status, what):
         if status != 0:
             raise self.fa.FAError(status, what)
@@ -544,6 +553,7 @@ def run_ours(args, w):
             pp = Problem(fa, torch, pw, dev, stream)
             pt = pp.time(torch, args.per_config_steps, 3, flush)
             per_config[name] = kernel_figures(pw, pt, peak)
+            per_config[name]["device_memory"] = pp.device_mib()
             del pp
             torch.cuda.empty_cache()
         per_config["clocks"] = pc_sampler.stop()
@@ -567,6 +577,7 @@ def run_ours(args, w):
                          "sustained_peak_source": peak_sus_src,
                          "traffic": ncu_traffic(dom, w.name),
                          "algorithmic_flops_per_launch": dom_flops},
+            "device_memory": prob.device_mib(),
             "per_config": per_config,
             "cpu_baseline": cpu,
             "e2e": e2e,
