@@ -136,11 +136,18 @@ def attention_forward(q, k, v, causal: bool, scale: float, row_block: int = 512,
 
 
 def attention_backward(q, k, v, do, causal: bool, scale: float, row_block: int = 512, row_range=None,
-                       window: int = 0):
+                       window: int = 0, o_for_d=None):
     """(dQ, dK, dV) of L = sum(dO * O) for exact attention, in fp64.
 
     ``row_range=(r0, r1)`` restricts the sum to query rows r0..r1-1: dQ rows
     outside it are zero and dK/dV hold only those rows' contributions.
+
+    ``o_for_d``: the backward recomputes from what the forward saved (the
+    output O and the log-sum-exp), so D_i = rowsum(P * dP) can be formed as
+    rowsum(dO * O), the same number in exact arithmetic (O = P V, so
+    dO_i . O_i = sum_j P_ij dO_i . v_j = sum_j P_ij dP_ij).  Given an O
+    [B, Hq, N, d] here (e.g. the forward's output rounded to bf16), D is
+    formed from it; by default D = rowsum(P * dP) from the exact P.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -164,7 +171,11 @@ def attention_backward(q, k, v, do, causal: bool, scale: float, row_block: int =
                 p, _, _ = _rows_of_p(q_blk, k[b, g], rows, N, causal, scale, window)
                 dv[b, g] += p.T @ do_blk
                 dp = do_blk @ v[b, g].T
-                ds = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
+                if o_for_d is None:
+                    drow = np.sum(p * dp, axis=1, keepdims=True)
+                else:
+                    drow = np.sum(do_blk * np.asarray(o_for_d[b, h, r0:r1], dtype=np.float64), axis=1, keepdims=True)
+                ds = p * (dp - drow)
                 dq[b, h, r0:r1] = scale * (ds @ k[b, g])
                 dk[b, g] += scale * (ds.T @ q_blk)
     return dq, dk, dv

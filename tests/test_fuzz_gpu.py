@@ -4,7 +4,7 @@ Each case draws, from one fixed seed: batch, kv heads and group size (GQA),
 query and key lengths (ragged, from 1 up to several tiles; fewer queries than
 keys for the decode-shaped forward, queries at the last positions), head dim
 64 or 128, causal or not, a sliding window (causal only), the number of key
-splits of the forward, the softmax scale (1/sqrt(d) or an arbitrary value),
+splits of the forward (1-6, more than the key tiles at small N), the softmax scale (1/sqrt(d) or an arbitrary value),
 the spread of q and k, and the deterministic or reduce-add backward.  Outputs
 live between guard bytes, so a write outside any output fails the case.
 
@@ -21,7 +21,7 @@ import torch
 import exact_io_aware_flashattention_gb300 as fa
 from exact_io_aware_flashattention_gb300.inputs import make_qkvdo, to_f64
 from oracle import ref
-from tests.parity import GuardedBuffers, assert_bwd, assert_fwd
+from tests.parity import GRAD_REL_L2, GuardedBuffers, as_f64, assert_bwd, assert_fwd, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -42,8 +42,7 @@ def draw_cases(n=N_CASES, seed=20261203):
         Nq = int(rng.integers(1, Nk + 1)) if decode else Nk
         causal = bool(rng.random() < 0.6)
         window = int(rng.integers(1, Nk + 1)) if causal and rng.random() < 0.4 else 0
-        n_key_tiles = -(-Nk // 128)
-        splits = int(rng.integers(1, min(4, n_key_tiles) + 1))
+        splits = int(rng.integers(1, 7))   # may exceed the key tiles: the library clamps
         scale = 1.0 / math.sqrt(d) if rng.random() < 0.5 else float(rng.uniform(0.02, 0.4))
         sigma = float(rng.choice([1.0, 2.0]))
         deterministic = bool(rng.random() < 0.4)
@@ -72,6 +71,7 @@ def test_cases_cover_the_features():
     assert any(c["Nq"] < c["Nk"] for c in CASES)
     assert any(c["window"] > 0 for c in CASES)
     assert any(c["splits"] > 1 for c in CASES)
+    assert any(c["splits"] > -(-c["Nk"] // 128) for c in CASES)
     assert any(c["deterministic"] and c["Nq"] == c["Nk"] for c in CASES)
     assert any(c["Nk"] % 128 != 0 and c["Nk"] > 128 for c in CASES)
     assert any(abs(c["scale"] - 1.0 / math.sqrt(c["d"])) > 1e-3 for c in CASES)
@@ -106,4 +106,16 @@ def test_fuzz_case(cuda_lib, c):
     assert_fwd(o, lse, ro, rlse, what)
     if grads is not None:
         rdq, rdk, rdv = ref.attention_backward(*args, to_f64(do), c["causal"], c["scale"], window=c["window"])
-        assert_bwd(*grads, rdq, rdk, rdv, what)
+        # The backward works from the saved bf16 O: D = rowsum(dO * O) carries
+        # O's rounding, which a row that sees few keys (dP - D cancels) turns
+        # into a dQ / dK error of its own.  The oracle with D from its O rounded
+        # to bf16 gives that floor; the CUDA path must match that reference
+        # within the tolerance, and the exact one within tolerance + floor.
+        ro_bf16 = torch.from_numpy(ro).to(torch.bfloat16).double().numpy()
+        fdq, fdk, fdv = ref.attention_backward(*args, to_f64(do), c["causal"], c["scale"], window=c["window"],
+                                               o_for_d=ro_bf16)
+        assert_bwd(*grads, fdq, fdk, fdv, what + " (D from bf16 O)")
+        for name, g, r, f in (("dq", grads[0], rdq, fdq), ("dk", grads[1], rdk, fdk), ("dv", grads[2], rdv, fdv)):
+            floor = rel_l2(f, r)
+            err = rel_l2(as_f64(g), r)
+            assert err <= GRAD_REL_L2 + floor, f"{what}: {name} rel-L2 {err} against the exact oracle (floor {floor})"

@@ -330,6 +330,24 @@ def test_d_identity():
         assert np.allclose((do[0, 0] * o[0, 0]).sum(1), (p * dp).sum(1), atol=1e-13)
 
 
+@pytest.mark.parametrize("causal,Hq,Hkv,window", [(False, 2, 1, 0), (True, 4, 2, 0), (True, 2, 2, 3)])
+def test_backward_with_d_from_the_output(causal, Hq, Hkv, window):
+    # The backward with D formed from the exact forward output (rowsum(dO * O))
+    # equals the default one (rowsum(P * dP)); with a perturbed output it differs,
+    # so the option is really used.
+    q = rand((2, Hq, 9, 6), 90)
+    k, v = rand((2, Hkv, 9, 6), 91), rand((2, Hkv, 9, 6), 92)
+    do = rand((2, Hq, 9, 6), 93)
+    o, _ = ref.attention_forward(q, k, v, causal, 0.4, window=window)
+    base = ref.attention_backward(q, k, v, do, causal, 0.4, window=window)
+    via_o = ref.attention_backward(q, k, v, do, causal, 0.4, window=window, o_for_d=o)
+    for x, y in zip(base, via_o):
+        assert np.allclose(x, y, rtol=1e-11, atol=1e-12)
+    bent = ref.attention_backward(q, k, v, do, causal, 0.4, window=window, o_for_d=o * (1 + 1e-3))
+    assert not np.allclose(bent[0], base[0], rtol=1e-6, atol=1e-9)
+    assert np.array_equal(bent[2], base[2])   # dV does not use D
+
+
 def test_stressed_logits_stay_finite():
     # Large logits (q, k ~ N(0, 3^2), as in the stressed workload) stay finite
     # because the max is subtracted before exp.
